@@ -1,0 +1,220 @@
+/*
+ * gq.h -- C ABI of the grouped FP8 quantizer and grouped expert GEMMs for
+ * MoE training on GB300 (sm_103a).
+ *
+ * The hot path has two parts:
+ *   1. gq_quantize: a bf16 token buffer partitioned by split_sizes is cast to
+ *      FP8 e4m3 with per-block scales, rowwise and/or columnwise.  Two
+ *      recipes: MXFP8 1x32 with E8M0 scales in the swizzled
+ *      [outer/128][inner/128][32][4][4] layout (TransformerEngine issue 3484,
+ *      "Describe the bug"; TransformerEngine PR 3224, the group_quantize_mxfp8
+ *      fix), and a per-channel 128-row fp32-scale recipe (DeepGEMM issue 365,
+ *      _per_channel_cast_to_fp8).
+ *   2. gq_gemm_fprop / gq_gemm_dgrad / gq_gemm_wgrad: grouped GEMMs that
+ *      consume those operands; the wgrad contracts only over each group's
+ *      live rows (TransformerEngine issue 3484, "Additional context: Scope").
+ *
+ * Conventions shared by every call
+ *  - Pointers named d_* and every buffer inside gq_quantized are DEVICE
+ *    pointers; descriptor structs themselves live in HOST memory.  The caller
+ *    owns all memory; the library allocates no device memory.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and never synchronises with the host, so a sequence of calls
+ *    can be captured in a CUDA graph once each (device, shape) pair has been
+ *    called once outside capture.
+ *  - Buffers are row-major.  A token buffer has rows_cap rows R; group g
+ *    owns rows [o_g, o_g + m_g) with o_g = m_0 + ... + m_{g-1} and
+ *    L = sum(m_g) <= R.  Rows >= L are padding: never read, never written,
+ *    and their content (zeros, garbage, NaN) never affects any result.
+ *  - split sizes: `d_split_sizes` is a device int32[num_groups]; NULL means
+ *    the uniform split m_g = rows_cap / num_groups (rows_cap must divide;
+ *    this is the single-grouped-weight case of TransformerEngine PR 3224).
+ *    MX needs every m_g % 32 == 0, the per-channel recipe m_g % 128 == 0;
+ *    all column counts must be multiples of 128.  1 <= num_groups <= 1024.
+ *  - Errors found on the host are returned synchronously and launch nothing.
+ *    Errors found on the device (split sizes: negative, misaligned, or
+ *    summing past rows_cap; a pipeline wait that timed out) are written to
+ *    *d_status (first error wins) and the kernel leaves its outputs
+ *    untouched.  Every kernel of every call first reads *d_status and does
+ *    nothing when it is nonzero, so one bad split table turns the rest of a
+ *    stream-ordered sequence into no-ops (the noop-flag semantics of
+ *    TransformerEngine PR 3224's group_quantize).  The caller zeroes
+ *    *d_status before a sequence and reads it afterwards.
+ *  - L == 0 (every group empty) dereferences no data pointer (PR 3224's
+ *    zero-row guard); the wgrad with accumulate == 0 still writes zeros.
+ */
+#ifndef GQ_H_
+#define GQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* gq_stream_t;
+
+typedef enum gq_status {
+    GQ_OK = 0,
+    GQ_ERR_INVALID_ARG = -1,    /* null pointer, bad count, capacity too small */
+    GQ_ERR_ALIGNMENT = -2,      /* cols % 128, rows_cap % num_groups, pointer alignment */
+    GQ_ERR_SPLITS = -3,         /* (device) a split is negative, misaligned, or they overflow rows_cap */
+    GQ_ERR_UNSUPPORTED = -4,    /* recipe / orientation / dtype combination not provided */
+    GQ_ERR_CUDA = -5,           /* a CUDA runtime call or launch failed */
+    GQ_ERR_TIMEOUT = -6,        /* (device) a pipeline wait gave up; outputs are undefined */
+    GQ_ERR_SHAPE_MISMATCH = -7  /* descriptor disagrees with the call (groups, rows, cols, recipe) */
+} gq_status;
+
+typedef enum gq_recipe_kind {
+    /* MXFP8 1x32: one E8M0 scale 2^e per 32 elements, e = floor(log2 amax) - 8
+     * clamped to [-127, 127] (an all-zero block gets e = -127, byte 0);
+     * codes = e4m3(x * 2^-e), nearest-even, saturating to +-448. */
+    GQ_RECIPE_MXFP8_1X32 = 0,
+    /* Per-channel 128-row fp32 scale (columnwise only), computed op by op in
+     * fp32: sf = amax / 448; sf == 0 -> zero_scale; sf = max(sf, 1e-30);
+     * codes = e4m3(x * (1 / sf)). */
+    GQ_RECIPE_CHANNEL128_F32 = 1
+} gq_recipe_kind;
+
+typedef enum gq_dtype { GQ_DTYPE_F32 = 0, GQ_DTYPE_BF16 = 1 } gq_dtype;
+
+typedef struct gq_recipe {
+    int32_t kind;        /* gq_recipe_kind */
+    int32_t rowwise;     /* 1: produce rowwise codes + scales (MX only) */
+    int32_t colwise;     /* 1: produce columnwise codes + scales */
+    float zero_scale;    /* per-channel recipe: the scale of an all-zero block (the
+                            page's sf_val); ignored by MX */
+} gq_recipe;
+
+/*
+ * A grouped quantised tensor (the GroupedTensor of TransformerEngine PR
+ * 3224), described by the caller and reusable across calls.
+ *
+ *  row_data / col_data : uint8 e4m3 codes, [rows_cap, cols] row-major.  Both
+ *      orientations keep the buffer's orientation: columnwise codes of row r
+ *      are stored in row r.  Only rows < L are written.
+ *  row_scale (MX) : uint8 E8M0 bytes.  Group g's region starts at byte
+ *      512 * (cols/128) * (T_0 + ... + T_{g-1}), T_h = ceil(m_h / 128), and
+ *      holds T_g * (cols/128) atoms of 512 bytes ordered [row tile][col tile].
+ *  col_scale (MX) : same region offsets; atoms ordered [col tile][row tile]:
+ *      the row (m) tile is the inner stride and its extent is the group's own
+ *      T_g, never the buffer's (TransformerEngine issue 3484).
+ *      Inside an atom, the scale of (row r of a 128-row tile, scale column j
+ *      of 4) -- for columnwise scales (channel r of a 128-channel tile,
+ *      32-row block j of 4) -- is byte (r % 32) * 16 + (r / 32) * 4 + j.
+ *      Entries of a group's last tile that cover no live row are 0.
+ *  col_scale (per-channel) : fp32 [L/128][cols]: the scale of live rows
+ *      [128 b, 128 b + 128) of channel c is element b * cols + c.
+ *  *_scale_bytes : capacity in bytes of each scale buffer (checked).
+ *
+ * Device buffers must be 16-byte aligned.
+ */
+typedef struct gq_quantized {
+    int32_t num_groups;
+    int32_t reserved0;
+    int64_t rows_cap;
+    int64_t cols;
+    gq_recipe recipe;
+    void* row_data;
+    void* row_scale;
+    void* col_data;
+    void* col_scale;
+    uint64_t row_scale_bytes;
+    uint64_t col_scale_bytes;
+} gq_quantized;
+
+/* Human-readable name of a status code (static storage). */
+const char* gq_status_string(int32_t status);
+
+/* ABI version, (major << 16) | minor. */
+int32_t gq_version(void);
+
+/* Bytes a scale buffer needs for any split table of num_groups groups over
+ * rows_cap rows: MX 512 * (cols/128) * (ceil(rows_cap/128) + num_groups);
+ * per-channel 4 * cols * (rows_cap / 128).  0 on a bad argument. */
+uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64_t rows_cap,
+                              int64_t cols);
+
+/*
+ * gq_split_scan -- the partition of a token buffer by split sizes
+ * (DeepGEMM issue 365, grouped_layout; TransformerEngine PR 3224, the m_splits
+ * alignment contract).  Writes d_table (device int64[3 * (num_groups + 1)]):
+ *   d_table[g]                     = o_g, the first row of group g (g = G: L)
+ *   d_table[(G + 1) + g]           = T_0 + ... + T_{g-1}, T_h = ceil(m_h / 128)
+ *   d_table[2 (G + 1) + g]         = byte offset of group g's scale region
+ *                                    (MX: 512 (cols/128) sum T; per-channel:
+ *                                    4 cols o_g / 128)
+ * Split errors go to *d_status and leave d_table untouched.  Every other
+ * call performs this scan inside its own kernels; this entry point exposes
+ * it for callers that size or inspect buffers.
+ */
+gq_status gq_split_scan(const int32_t* d_split_sizes, int32_t num_groups, int64_t rows_cap,
+                        int64_t cols, int32_t recipe_kind, int64_t* d_table, int32_t* d_status,
+                        gq_stream_t stream);
+
+/*
+ * gq_quantize -- grouped quantisation of x_bf16 ([rows_cap, cols] bf16,
+ * device) into the caller-described `out` (TransformerEngine PR 3224: output
+ * reuse with num_tensors / logical-shape validation).
+ *   out->num_groups, rows_cap, cols and recipe.kind must equal the call's
+ *   (else GQ_ERR_SHAPE_MISMATCH); the orientations requested by `recipe`
+ *   must have non-null buffers whose scale capacity is at least
+ *   gq_scale_bytes_bound (else GQ_ERR_INVALID_ARG).  out->recipe is
+ *   overwritten with *recipe.
+ * Reads rows < L of x only; writes codes of rows < L and the grouped scale
+ * regions (bytes past the last group's region are untouched).
+ */
+gq_status gq_quantize(const void* x_bf16, int64_t rows_cap, int64_t cols,
+                      const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
+                      gq_quantized* out, int32_t* d_status, gq_stream_t stream);
+
+/*
+ * gq_gemm_fprop -- Y_g = X_g W_g^T for every group g (TransformerEngine PR
+ * 3224, general_grouped_gemm_for_grouped_tensor in the forward sequence).
+ *   x : MX rowwise, rows_cap R, cols k, split by d_split_sizes.
+ *   w : MX rowwise, rows_cap num_groups * n, cols k, uniform split (W_g is
+ *       rows [g n, g n + n)).
+ *   y : [R, n] of out_dtype (GQ_DTYPE_F32 or GQ_DTYPE_BF16, nearest-even);
+ *       rows < L written, rows >= L untouched.
+ * n and k must be multiples of 128.
+ */
+gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
+                        const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                        void* y, int32_t out_dtype, int32_t* d_status, gq_stream_t stream);
+
+/*
+ * gq_gemm_dgrad -- dX_g = dY_g W_g (TransformerEngine issue 3484: M is a
+ * free dimension of the dgrad).
+ *   dy : MX rowwise, rows_cap R, cols n.
+ *   w  : MX columnwise (32-row blocks along n, group-local layout), rows_cap
+ *        num_groups * n, cols k.
+ *   dx : [R, k] of out_dtype; rows < L written.
+ */
+gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
+                        const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                        void* dx, int32_t out_dtype, int32_t* d_status, gq_stream_t stream);
+
+/*
+ * gq_gemm_wgrad -- k-grouped weight gradient
+ *   dW_g = (accumulate ? dW_g : 0) + dY_g^T X_g
+ * contracting over group g's live rows only (TransformerEngine issue 3484;
+ * DeepGEMM issue 365, k_grouped_fp8_gemm_nt_contiguous with recipe (1,1,128)).
+ *   dy, x : both MX columnwise, or both per-channel; rows_cap R; cols n and k.
+ *   dw    : fp32 [num_groups, n, k].  accumulate = 1 adds into it (the
+ *           accumulate_into_main_grad of TransformerEngine issue 3484); an
+ *           empty group then leaves dW_g bit-unchanged, with accumulate = 0
+ *           it writes +0.0.
+ * Deterministic: every output element is produced by one CTA in a fixed
+ * order; repeated calls give bitwise identical results.
+ */
+gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
+                        const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                        float* dw, int32_t accumulate, int32_t* d_status, gq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H_ */

@@ -1,0 +1,801 @@
+// Grouped FP8 GEMMs on the 5th-generation tensor core (tcgen05, sm_103a).
+//
+//  fprop  Y_g  = X_g W_g^T      A = X rowwise (K-major), B = W_g rowwise (K-major)
+//  dgrad  dX_g = dY_g W_g       A = dY rowwise (K-major), B = W_g columnwise (MN-major)
+//  wgrad  dW_g = dY_g^T X_g     A = dY columnwise (MN-major), B = X columnwise (MN-major),
+//                               contracting over group g's live rows only
+//
+// (TransformerEngine issue 3484: forward and dgrad have M as a free
+// dimension, the wgrad contracts over the token axis; DeepGEMM issue 365:
+// the k-grouped wgrad with per-channel 128-row fp32 scales.)
+//
+// One persistent CTA per SM walks a static tile list (tile = blockIdx.x +
+// i * gridDim.x).  Warp roles:
+//   warp 0 (one thread)  TMA producer: operand tiles by 2-D tensor maps with
+//                        128-byte swizzle, 512-byte E8M0 scale atoms by bulk
+//                        copies, into a ring of shared-memory stages;
+//   warp 1 (one thread)  MMA issuer: copies the scale atoms to TMEM
+//                        (tcgen05.cp), issues block-scaled MMAs
+//                        (kind::mxf8f6f4, M = 128, N = BN, K = 32 per
+//                        instruction, 4 per 128-deep k-tile), commits stages
+//                        back to the producer and finished accumulators to
+//                        the epilogue;
+//   warps 4..7           epilogue: TMEM -> registers -> global, one output
+//                        row per thread.
+// Accumulators live in TMEM (double-buffered for BN = 128) so the epilogue of
+// one tile overlaps the MMAs of the next.  Each output element is produced
+// by one CTA with a fixed contraction order: results are deterministic.
+//
+// The wgrad's last k-tile of a group with m_g % 128 != 0 issues only
+// m_g % 128 / 32 of its four MMAs, so rows past the group (the next group's
+// tokens, padding, or out-of-range zero fill) never enter a contraction.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "gq_internal.h"
+#include "gq_ptx.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int BM = 128;     // MMA M (rows of the A side)
+constexpr int BK = 128;     // k-tile depth in elements (= bytes for e4m3)
+constexpr int kSmemLimit = 227 * 1024;
+
+struct GemmArgs {
+    const int32_t* splits;
+    int G;
+    int64_t rows_cap;
+    int64_t n, k;             // the API's n and k
+    const uint8_t* sfa;       // scale base of the A-side operand
+    const uint8_t* sfb;       // scale base of the B-side operand
+    void* out;
+    int accumulate;
+    int32_t* status;
+};
+
+template <int BN>
+struct MxShape {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int SFA_BYTES = 512;
+    static constexpr int SFB_BYTES = 512 * (BN / 128);
+    static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
+    static constexpr uint32_t SFA_COL = ACC * BN;                     // TMEM column of A scales
+    static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1) + 16;
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - SCAN_BYTES - BAR_BYTES) / STAGE;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + SCAN_BYTES;
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+    static_assert(SFB_COL + BN / 32 <= TMEM_COLS, "TMEM budget");
+};
+
+// Shared-memory carve-up common to the GEMM kernels.
+struct Carve {
+    uint8_t* a;
+    uint8_t* b;
+    uint8_t* sfa;
+    uint8_t* sfb;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* tfull;
+    uint64_t* tempty;
+    uint64_t* drain;
+    uint32_t* tmem_base;
+    volatile int* abort;
+    int64_t* s_off;
+    int32_t* s_tp;
+    int64_t* s_w64;
+    int32_t* s_w32;
+};
+
+__device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, int b_bytes,
+                                       int sfa_bytes, int sfb_bytes, int acc)
+{
+    Carve c;
+    uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                            ~uintptr_t(1023));
+    c.a = p;
+    p += stages * a_bytes;
+    c.b = p;
+    p += stages * b_bytes;
+    c.sfa = p;
+    p += stages * sfa_bytes;
+    c.sfb = p;
+    p += stages * sfb_bytes;
+    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 7) & ~uintptr_t(7));
+    c.full = reinterpret_cast<uint64_t*>(p);
+    c.empty = c.full + 8;
+    c.tfull = c.empty + 8;
+    c.tempty = c.tfull + acc;
+    c.drain = c.tempty + acc;
+    c.tmem_base = reinterpret_cast<uint32_t*>(c.drain + 1);
+    c.abort = reinterpret_cast<volatile int*>(c.tmem_base + 1);
+    c.s_off = reinterpret_cast<int64_t*>(c.tmem_base + 4);
+    c.s_tp = reinterpret_cast<int32_t*>(c.s_off + GQ_MAX_GROUPS + 1);
+    c.s_w64 = reinterpret_cast<int64_t*>(c.s_tp + GQ_MAX_GROUPS + 2);
+    c.s_w32 = reinterpret_cast<int32_t*>(c.s_w64 + 32);
+    return c;
+}
+
+// One output tile of a grouped GEMM.
+struct Tile {
+    int g;            // group
+    int64_t row0;     // fprop/dgrad: first token row of the tile; wgrad: first token row of the group
+    int rows;         // fprop/dgrad: live rows in the tile (a multiple of 32)
+    int64_t mt;       // fprop/dgrad: row tile inside the group; wgrad: 128-row tile of n
+    int64_t col0;     // first output column
+    int nk;           // k-tiles
+    int last_sub;     // K = 32 steps in the last k-tile (wgrad), else 4
+    int T;            // 128-row tiles of the group
+    bool skip;        // nothing to do (empty group, accumulate)
+};
+
+template <int KIND, int BN>
+__device__ __forceinline__ int64_t tile_count(const GemmArgs& p, const int32_t* s_tp)
+{
+    if (KIND == GEMM_FPROP)
+        return (int64_t)s_tp[p.G] * (p.n / BN);
+    if (KIND == GEMM_DGRAD)
+        return (int64_t)s_tp[p.G] * (p.k / BN);
+    return (int64_t)p.G * (p.n / BM) * (p.k / BN);
+}
+
+template <int KIND, int BN>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& p, const int64_t* s_off,
+                                            const int32_t* s_tp, int64_t tile)
+{
+    Tile t;
+    if (KIND == GEMM_FPROP || KIND == GEMM_DGRAD) {
+        const int64_t nnt = (KIND == GEMM_FPROP ? p.n : p.k) / BN;
+        const int64_t rt = tile / nnt;
+        const int64_t nt = tile - rt * nnt;
+        t.g = group_of_tile(s_tp, p.G, rt);
+        t.mt = rt - s_tp[t.g];
+        const int64_t m = s_off[t.g + 1] - s_off[t.g];
+        t.row0 = s_off[t.g] + 128 * t.mt;
+        t.rows = (int)min((int64_t)128, m - 128 * t.mt);
+        t.col0 = nt * BN;
+        t.nk = (int)((KIND == GEMM_FPROP ? p.k : p.n) / BK);
+        t.last_sub = 4;
+        t.T = s_tp[t.g + 1] - s_tp[t.g];
+        t.skip = false;
+    } else {
+        const int64_t nkt = p.k / BN;
+        const int64_t per_group = (p.n / BM) * nkt;
+        t.g = (int)(tile / per_group);
+        const int64_t rem = tile - (int64_t)t.g * per_group;
+        t.mt = rem / nkt;
+        t.col0 = (rem - t.mt * nkt) * BN;
+        const int64_t m = s_off[t.g + 1] - s_off[t.g];
+        t.row0 = s_off[t.g];
+        t.rows = 128;
+        t.nk = (int)((m + 127) / 128);
+        t.last_sub = t.nk > 0 ? (int)((m - 128 * (int64_t)(t.nk - 1)) / 32) : 0;
+        t.T = s_tp[t.g + 1] - s_tp[t.g];
+        t.skip = (m == 0) && p.accumulate;
+    }
+    return t;
+}
+
+__device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&r)[32])
+{
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+}
+
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t (&r)[32])
+{
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * j]),
+                                                           __uint_as_float(r[8 * i + 2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__device__ __forceinline__ void accumulate_row_f32(float* dst, const uint32_t (&r)[32])
+{
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 o = d[i];
+        d[i] = make_float4(o.x + __uint_as_float(r[4 * i]), o.y + __uint_as_float(r[4 * i + 1]),
+                           o.z + __uint_as_float(r[4 * i + 2]), o.w + __uint_as_float(r[4 * i + 3]));
+    }
+}
+
+// Wait for the TMA writes of the last min(stages, issued) issued stages, so
+// that none lands after the CTA has left (bounded; used on every exit path).
+__device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t issued,
+                                            int32_t* status)
+{
+    volatile int no_abort = 0;
+    for (int64_t q = issued - stages < 0 ? 0 : issued - stages; q < issued; ++q)
+        if (!ptx::mbar_wait(&full[q % stages], (uint32_t)((q / stages) & 1), &no_abort, status))
+            break;
+}
+
+// ------------------------------------------------------------------------ //
+// MXFP8 grouped GEMM (fprop, dgrad, wgrad)                                  //
+// ------------------------------------------------------------------------ //
+
+template <int KIND, int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(256, 1)
+k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+          const GemmArgs p)
+{
+    using S = MxShape<BN>;
+    constexpr bool A_MN = (KIND == GEMM_WGRAD_MX);
+    constexpr bool B_MN = (KIND != GEMM_FPROP);
+    extern __shared__ uint8_t smem_raw[];
+    const Carve c = carve(smem_raw, S::STAGES, S::A_BYTES, S::B_BYTES, S::SFA_BYTES, S::SFB_BYTES,
+                          S::ACC);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (load_status(p.status) != 0)
+        return;
+    const int err = block_scan_splits(p.splits, p.G, p.rows_cap, 32, c.s_off, c.s_tp, c.s_w64,
+                                      c.s_w32);
+    if (err) {
+        if (threadIdx.x == 0)
+            set_status(p.status, err);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::STAGES; ++s) {
+            ptx::mbar_init(&c.full[s], 1);
+            ptx::mbar_init(&c.empty[s], 1);
+        }
+        for (int a = 0; a < S::ACC; ++a) {
+            ptx::mbar_init(&c.tfull[a], 1);
+            ptx::mbar_init(&c.tempty[a], 4);
+        }
+        ptx::mbar_init(c.drain, 1);
+        *c.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(c.tmem_base, S::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tma_a);
+        ptx::prefetch_tmap(&tma_b);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *c.tmem_base;
+    const int64_t ntiles = tile_count<KIND, BN>(p, c.s_tp);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer --
+        int64_t issued = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip || t.nk == 0)
+                continue;
+            for (int kt = 0; kt < t.nk; ++kt, ++issued) {
+                const int s = (int)(issued % S::STAGES);
+                const uint32_t ph = (uint32_t)((issued / S::STAGES) & 1);
+                if (!ptx::mbar_wait(&c.empty[s], ph ^ 1u, c.abort, p.status))
+                    break;
+                uint64_t* bar = &c.full[s];
+                ptx::mbar_arrive_expect_tx(bar, S::STAGE);
+                uint8_t* sa = c.a + s * S::A_BYTES;
+                uint8_t* sb = c.b + s * S::B_BYTES;
+                uint8_t* ssfa = c.sfa + s * S::SFA_BYTES;
+                uint8_t* ssfb = c.sfb + s * S::SFB_BYTES;
+                if (KIND == GEMM_FPROP) {
+                    const int64_t kb = p.k / 128;
+                    ptx::tma_load_2d(sa, &tma_a, bar, kt * BK, (int32_t)t.row0);
+                    ptx::tma_load_2d(sb, &tma_b, bar, kt * BK, (int32_t)(t.g * p.n + t.col0));
+                    ptx::bulk_load(ssfa, p.sfa + 512 * (kb * c.s_tp[t.g] + t.mt * kb + kt), 512, bar);
+                    const int64_t wbase = kb * (int64_t)t.g * (p.n / 128);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::bulk_load(ssfb + 512 * j,
+                                       p.sfb + 512 * (wbase + (t.col0 / 128 + j) * kb + kt), 512, bar);
+                } else if (KIND == GEMM_DGRAD) {
+                    const int64_t nb = p.n / 128;
+                    ptx::tma_load_2d(sa, &tma_a, bar, kt * BK, (int32_t)t.row0);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::tma_load_2d(sb + 16384 * j, &tma_b, bar, (int32_t)(t.col0 + 128 * j),
+                                         (int32_t)(t.g * p.n + kt * BK));
+                    ptx::bulk_load(ssfa, p.sfa + 512 * (nb * c.s_tp[t.g] + t.mt * nb + kt), 512, bar);
+                    const int64_t wbase = (p.k / 128) * (int64_t)t.g * nb;
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::bulk_load(ssfb + 512 * j,
+                                       p.sfb + 512 * (wbase + (t.col0 / 128 + j) * nb + kt), 512, bar);
+                } else {
+                    const int32_t r = (int32_t)(t.row0 + (int64_t)kt * BK);
+                    ptx::tma_load_2d(sa, &tma_a, bar, (int32_t)(t.mt * BM), r);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::tma_load_2d(sb + 16384 * j, &tma_b, bar, (int32_t)(t.col0 + 128 * j), r);
+                    ptx::bulk_load(ssfa,
+                                   p.sfa + 512 * ((p.n / 128) * c.s_tp[t.g] + t.mt * t.T + kt), 512,
+                                   bar);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::bulk_load(ssfb + 512 * j,
+                                       p.sfb + 512 * ((p.k / 128) * c.s_tp[t.g] +
+                                                      (t.col0 / 128 + j) * t.T + kt),
+                                       512, bar);
+                }
+            }
+        }
+        drain_loads(c.full, S::STAGES, issued, p.status);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------- MMA issuer --
+        int64_t consumed = 0, tiles_done = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip || t.nk == 0)
+                continue;
+            const int acc = (int)(tiles_done % S::ACC);
+            const uint32_t acc_ph = (uint32_t)((tiles_done / S::ACC) & 1);
+            if (!ptx::mbar_wait(&c.tempty[acc], acc_ph ^ 1u, c.abort, p.status))
+                break;
+            ptx::tc_fence_after_sync();
+            const uint32_t d = tmem + acc * BN;
+            bool ok = true;
+            for (int kt = 0; kt < t.nk; ++kt, ++consumed) {
+                const int s = (int)(consumed % S::STAGES);
+                const uint32_t ph = (uint32_t)((consumed / S::STAGES) & 1);
+                if (!ptx::mbar_wait(&c.full[s], ph, c.abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                ptx::tc_cp_sf_atom(tmem + S::SFA_COL,
+                                   ptx::smem_desc(ptx::smem_addr(c.sfa + s * S::SFA_BYTES), 0, 128, 0));
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+                    ptx::tc_cp_sf_atom(tmem + S::SFB_COL + 4 * j,
+                                       ptx::smem_desc(ptx::smem_addr(c.sfb + s * S::SFB_BYTES + 512 * j),
+                                                      0, 128, 0));
+                const uint32_t a_addr = ptx::smem_addr(c.a + s * S::A_BYTES);
+                const uint32_t b_addr = ptx::smem_addr(c.b + s * S::B_BYTES);
+                const int nsub = (kt == t.nk - 1) ? t.last_sub : 4;
+                for (int j = 0; j < nsub; ++j) {
+                    // K-major: step 32 bytes along the swizzled 128-byte row;
+                    // MN-major: step 32 rows of 128 bytes.
+                    const uint64_t ad = A_MN ? ptx::smem_desc(a_addr + 4096 * j, 16384, 1024, 2)
+                                             : ptx::smem_desc(a_addr + 32 * j, 16, 1024, 2);
+                    const uint64_t bd = B_MN ? ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2)
+                                             : ptx::smem_desc(b_addr + 32 * j, 16, 1024, 2);
+                    ptx::tc_mma_mxf8(d, ad, bd, ptx::idesc_mxf8(BM, BN, A_MN, B_MN, (uint32_t)j),
+                                     tmem + S::SFA_COL, tmem + S::SFB_COL, (kt | j) != 0);
+                }
+                ptx::tc_commit(&c.empty[s]);
+            }
+            if (!ok)
+                break;
+            ptx::tc_commit(&c.tfull[acc]);
+            ++tiles_done;
+        }
+        ptx::tc_commit(c.drain);
+        volatile int no_abort = 0;
+        ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
+    } else if (warp >= 4) {
+        // --------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const int r = 32 * q + lane;        // row of the tile this thread writes
+        int64_t tiles_done = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip)
+                continue;
+            float* out32 = nullptr;
+            uint16_t* out16 = nullptr;
+            if (KIND == GEMM_FPROP || KIND == GEMM_DGRAD) {
+                const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
+                if (OUT_BF16)
+                    out16 = static_cast<uint16_t*>(p.out) + (t.row0 + r) * ld + t.col0;
+                else
+                    out32 = static_cast<float*>(p.out) + (t.row0 + r) * ld + t.col0;
+            } else {
+                out32 = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k + t.col0;
+            }
+            if (t.nk == 0) {                 // empty group, accumulate == 0: write +0.0
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < BN / 4; ++i)
+                    reinterpret_cast<float4*>(out32)[i] = z;
+                continue;
+            }
+            const int acc = (int)(tiles_done % S::ACC);
+            const uint32_t acc_ph = (uint32_t)((tiles_done / S::ACC) & 1);
+            if (!ptx::mbar_wait(&c.tfull[acc], acc_ph, c.abort, p.status))
+                break;
+            ptx::tc_fence_after_sync();
+            const bool live = r < t.rows;
+            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32(base + 32 * cc, v);
+                ptx::tmem_wait_ld(v);
+                if (live) {
+                    if (OUT_BF16)
+                        store_row_bf16(out16 + 32 * cc, v);
+                    else if (KIND == GEMM_WGRAD_MX && p.accumulate)
+                        accumulate_row_f32(out32 + 32 * cc, v);
+                    else
+                        store_row_f32(out32 + 32 * cc, v);
+                }
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&c.tempty[acc]);
+            ++tiles_done;
+        }
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------ //
+// Per-channel 128-row fp32-scale k-grouped wgrad                            //
+// ------------------------------------------------------------------------ //
+//
+// dW_g[i, j] = sum_b sfA[b, i] sfB[b, j] sum_{t in block b} qA[t, i] qB[t, j]
+// Each 128-token block's unscaled partial (kind::f8f6f4) goes to one of two
+// TMEM buffers; the epilogue (two warpgroups, 64 columns each) promotes it
+// by the outer product of the block's channel scales into fp32 registers.
+// The partial buffer is handed back only after its tcgen05.ld has completed
+// (commit -> full, wait::ld -> fence -> arrive empty), so a partial is never
+// overwritten while being read.
+
+struct ChShape {
+    static constexpr int BN = 128;
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int PBUF = 2;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr int SCAN_BYTES = MxShape<128>::SCAN_BYTES;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * PBUF + 1) + 16;
+    static constexpr int STAGES = 6;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + SCAN_BYTES;
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(384, 1)
+k_gemm_wgrad_channel(const __grid_constant__ CUtensorMap tma_a,
+                     const __grid_constant__ CUtensorMap tma_b, const GemmArgs p)
+{
+    using S = ChShape;
+    constexpr int BN = S::BN;
+    extern __shared__ uint8_t smem_raw[];
+    const Carve c = carve(smem_raw, S::STAGES, S::A_BYTES, S::B_BYTES, 0, 0, S::PBUF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* sfa = reinterpret_cast<const float*>(p.sfa);
+    const float* sfb = reinterpret_cast<const float*>(p.sfb);
+
+    if (load_status(p.status) != 0)
+        return;
+    const int err = block_scan_splits(p.splits, p.G, p.rows_cap, 128, c.s_off, c.s_tp, c.s_w64,
+                                      c.s_w32);
+    if (err) {
+        if (threadIdx.x == 0)
+            set_status(p.status, err);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::STAGES; ++s) {
+            ptx::mbar_init(&c.full[s], 1);
+            ptx::mbar_init(&c.empty[s], 1);
+        }
+        for (int a = 0; a < S::PBUF; ++a) {
+            ptx::mbar_init(&c.tfull[a], 1);
+            ptx::mbar_init(&c.tempty[a], 8);
+        }
+        ptx::mbar_init(c.drain, 1);
+        *c.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(c.tmem_base, S::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tma_a);
+        ptx::prefetch_tmap(&tma_b);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *c.tmem_base;
+    const int64_t ntiles = tile_count<GEMM_WGRAD_CHANNEL, BN>(p, c.s_tp);
+
+    if (warp == 0 && lane == 0) {
+        int64_t issued = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<GEMM_WGRAD_CHANNEL, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip || t.nk == 0)
+                continue;
+            for (int kt = 0; kt < t.nk; ++kt, ++issued) {
+                const int s = (int)(issued % S::STAGES);
+                const uint32_t ph = (uint32_t)((issued / S::STAGES) & 1);
+                if (!ptx::mbar_wait(&c.empty[s], ph ^ 1u, c.abort, p.status))
+                    break;
+                uint64_t* bar = &c.full[s];
+                ptx::mbar_arrive_expect_tx(bar, S::STAGE);
+                const int32_t r = (int32_t)(t.row0 + (int64_t)kt * BK);
+                ptx::tma_load_2d(c.a + s * S::A_BYTES, &tma_a, bar, (int32_t)(t.mt * BM), r);
+                ptx::tma_load_2d(c.b + s * S::B_BYTES, &tma_b, bar, (int32_t)t.col0, r);
+            }
+        }
+        drain_loads(c.full, S::STAGES, issued, p.status);
+    } else if (warp == 1 && lane == 0) {
+        int64_t consumed = 0, parts = 0;
+        constexpr uint32_t idesc = ptx::idesc_f8(BM, BN, 1, 1);
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<GEMM_WGRAD_CHANNEL, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip || t.nk == 0)
+                continue;
+            bool ok = true;
+            for (int kt = 0; kt < t.nk && ok; ++kt, ++consumed, ++parts) {
+                const int pb = (int)(parts % S::PBUF);
+                const uint32_t pph = (uint32_t)((parts / S::PBUF) & 1);
+                const int s = (int)(consumed % S::STAGES);
+                const uint32_t ph = (uint32_t)((consumed / S::STAGES) & 1);
+                if (!ptx::mbar_wait(&c.tempty[pb], pph ^ 1u, c.abort, p.status) ||
+                    !ptx::mbar_wait(&c.full[s], ph, c.abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t a_addr = ptx::smem_addr(c.a + s * S::A_BYTES);
+                const uint32_t b_addr = ptx::smem_addr(c.b + s * S::B_BYTES);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    ptx::tc_mma_f8(tmem + pb * BN, ptx::smem_desc(a_addr + 4096 * j, 16384, 1024, 2),
+                                   ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2), idesc, j != 0);
+                ptx::tc_commit(&c.empty[s]);
+                ptx::tc_commit(&c.tfull[pb]);
+            }
+            if (!ok)
+                break;
+        }
+        ptx::tc_commit(c.drain);
+        volatile int no_abort = 0;
+        ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
+    } else if (warp >= 4) {
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        const int r = 32 * q + lane;
+        int64_t parts = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<GEMM_WGRAD_CHANNEL, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip)
+                continue;
+            const int64_t n_row = t.mt * BM + r;                       // output row (channel of dY)
+            const int64_t col = t.col0 + 64 * h;                       // first output column
+            float* out = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + n_row) * p.k + col;
+            float acc[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                acc[i] = 0.f;
+            bool ok = true;
+            for (int kt = 0; kt < t.nk; ++kt, ++parts) {
+                const int pb = (int)(parts % S::PBUF);
+                const uint32_t pph = (uint32_t)((parts / S::PBUF) & 1);
+                if (!ptx::mbar_wait(&c.tfull[pb], pph, c.abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + pb * BN + 64 * h;
+                uint32_t v0[32], v1[32];
+                ptx::tmem_ld_32x32(base, v0);
+                ptx::tmem_ld_32x32(base + 32, v1);
+                ptx::tmem_wait_ld(v0);
+                ptx::tmem_wait_ld(v1);
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(&c.tempty[pb]);
+                const int64_t b = (t.row0 >> 7) + kt;                    // global 128-row block
+                const float sa = __ldg(sfa + b * p.n + n_row);
+                const float4* sb4 = reinterpret_cast<const float4*>(sfb + b * p.k + col);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 s = __ldg(sb4 + i);
+                    acc[4 * i + 0] = fmaf(sa * s.x, __uint_as_float(v0[4 * i + 0]), acc[4 * i + 0]);
+                    acc[4 * i + 1] = fmaf(sa * s.y, __uint_as_float(v0[4 * i + 1]), acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(sa * s.z, __uint_as_float(v0[4 * i + 2]), acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(sa * s.w, __uint_as_float(v0[4 * i + 3]), acc[4 * i + 3]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 s = __ldg(sb4 + 8 + i);
+                    acc[32 + 4 * i + 0] = fmaf(sa * s.x, __uint_as_float(v1[4 * i + 0]), acc[32 + 4 * i + 0]);
+                    acc[32 + 4 * i + 1] = fmaf(sa * s.y, __uint_as_float(v1[4 * i + 1]), acc[32 + 4 * i + 1]);
+                    acc[32 + 4 * i + 2] = fmaf(sa * s.z, __uint_as_float(v1[4 * i + 2]), acc[32 + 4 * i + 2]);
+                    acc[32 + 4 * i + 3] = fmaf(sa * s.w, __uint_as_float(v1[4 * i + 3]), acc[32 + 4 * i + 3]);
+                }
+            }
+            if (!ok)
+                break;
+            float4* o = reinterpret_cast<float4*>(out);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float4 v = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                if (p.accumulate) {
+                    const float4 old = o[i];
+                    v = make_float4(old.x + v.x, old.y + v.y, old.z + v.z, old.w + v.w);
+                }
+                o[i] = v;
+            }
+        }
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+}
+
+// Zero-fill of dW for a wgrad over an empty buffer (no operand to map).
+__global__ void k_zero_fill(float* __restrict__ out, int64_t count, const int32_t* status)
+{
+    if (load_status(status) != 0)
+        return;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = 0.f;
+}
+
+// ------------------------------------------------------------------------ //
+// Host side                                                                 //
+// ------------------------------------------------------------------------ //
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a row-major uint8 [rows, cols] buffer with boxes of 128
+// columns x box_rows rows and 128-byte swizzle; out-of-range rows read 0.
+bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t cols, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename Kernel>
+cudaError_t prepare(Kernel kernel, int smem)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int KIND, int BN, bool OUT_BF16>
+gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
+                 int64_t tiles_bound, cudaStream_t stream)
+{
+    using S = MxShape<BN>;
+    auto kernel = k_gemm_mx<KIND, BN, OUT_BF16>;
+    if (prepare(kernel, S::SMEM) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
+    kernel<<<(unsigned)grid, 256, S::SMEM, stream>>>(ma, mb, args);
+    return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+}
+
+}  // namespace
+
+gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
+                      const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
+                      void* out, int out_dtype, int accumulate, int32_t* status,
+                      cudaStream_t stream)
+{
+    GemmArgs args;
+    args.splits = splits;
+    args.G = G;
+    args.rows_cap = rows_cap;
+    args.n = n;
+    args.k = k;
+    args.sfa = static_cast<const uint8_t*>(a.scale);
+    args.sfb = static_cast<const uint8_t*>(b.scale);
+    args.out = out;
+    args.accumulate = accumulate;
+    args.status = status;
+
+    if (rows_cap >= (int64_t(1) << 31) || b.rows >= (int64_t(1) << 31))
+        return GQ_ERR_INVALID_ARG;
+    if (rows_cap == 0) {            // wgrad over an empty buffer: dW = 0 or unchanged
+        if (!accumulate) {
+            k_zero_fill<<<256, 256, 0, stream>>>(static_cast<float*>(out), (int64_t)G * n * k, status);
+            return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+        }
+        return GQ_OK;
+    }
+    CUtensorMap ma, mb;
+    switch (kind) {
+    case GEMM_FPROP: {
+        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+            return GQ_ERR_CUDA;
+        const int64_t bound = ((rows_cap + 127) / 128 + G) * (n / 128);
+        return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_FPROP, 128, true>(ma, mb, args, bound, stream)
+                                          : run_mx<GEMM_FPROP, 128, false>(ma, mb, args, bound, stream);
+    }
+    case GEMM_DGRAD: {
+        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+            return GQ_ERR_CUDA;
+        const int64_t bound = ((rows_cap + 127) / 128 + G) * (k / 128);
+        return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_DGRAD, 128, true>(ma, mb, args, bound, stream)
+                                          : run_mx<GEMM_DGRAD, 128, false>(ma, mb, args, bound, stream);
+    }
+    case GEMM_WGRAD_MX: {
+        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+            return GQ_ERR_CUDA;
+        const int64_t bound = (int64_t)G * (n / 128) * (k / 128);
+        return run_mx<GEMM_WGRAD_MX, 128, false>(ma, mb, args, bound, stream);
+    }
+    case GEMM_WGRAD_CHANNEL: {
+        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+            return GQ_ERR_CUDA;
+        if (prepare(k_gemm_wgrad_channel, ChShape::SMEM) != cudaSuccess)
+            return GQ_ERR_CUDA;
+        const int64_t bound = (int64_t)G * (n / 128) * (k / 128);
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(bound, device_info().sm_count));
+        k_gemm_wgrad_channel<<<(unsigned)grid, 384, ChShape::SMEM, stream>>>(ma, mb, args);
+        return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+    }
+    }
+    return GQ_ERR_UNSUPPORTED;
+}
+
+}  // namespace gq

@@ -1,0 +1,48 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gq.h"
+
+#define GQ_MAX_GROUPS 1024
+
+namespace gq {
+
+// Per-device facts, queried once per device.
+struct DeviceInfo {
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+};
+const DeviceInfo& device_info();
+
+// Quantizer launchers (gq_quant.cu).
+cudaError_t launch_split_scan(const int32_t* splits, int G, int64_t rows_cap, int64_t cols,
+                              int align, int scale_kind, int64_t* table, int32_t* status,
+                              cudaStream_t stream);
+cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const int32_t* splits,
+                            int G, uint8_t* row_data, uint8_t* row_scale, uint8_t* col_data,
+                            uint8_t* col_scale, int32_t* status, cudaStream_t stream);
+cudaError_t launch_quant_channel(const void* x, int64_t rows_cap, int64_t cols,
+                                 const int32_t* splits, int G, float zero_scale,
+                                 uint8_t* col_data, float* col_scale, int32_t* status,
+                                 cudaStream_t stream);
+
+// GEMM launchers (gq_gemm.cu).  Operand buffers are already validated.
+struct GemmOperand {
+    const uint8_t* data;   // e4m3 codes [rows, cols]
+    const void* scale;     // E8M0 swizzled bytes or fp32 per-channel scales
+    int64_t rows;          // rows of the buffer (rows_cap, or G * n for weights)
+    int64_t cols;
+};
+enum GemmKind { GEMM_FPROP = 0, GEMM_DGRAD = 1, GEMM_WGRAD_MX = 2, GEMM_WGRAD_CHANNEL = 3 };
+
+gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
+                      const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
+                      void* out, int out_dtype, int accumulate, int32_t* status,
+                      cudaStream_t stream);
+
+}  // namespace gq
