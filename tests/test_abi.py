@@ -1,0 +1,123 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports
+every function include/gq.h declares, and its host-side checks answer before
+anything is launched.  No call here reaches a kernel launch: every call either
+fails a host check or touches no device pointer."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import moe_grouped_gemm_group_gb300 as gq
+from moe_grouped_gemm_group_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return gq.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("gq_quantize", "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_split_scan"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", gq.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, f"{name} not exported (C linkage) by libgq.so"
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    assert gq.gq_version() >> 16 == 1
+    for code, name in gq.STATUS.items():
+        assert gq.gq_status_string(code).startswith(name)
+    assert "unknown" in gq.gq_status_string(12345)
+
+
+def test_scale_bytes_bound(lib):
+    mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    ch = gq.Recipe(gq.RECIPE_CHANNEL128_F32, 0, 1, 1e-30)
+    assert gq.gq_scale_bytes_bound(mx, 64, 66560, 7168) == 512 * 56 * (520 + 64)
+    assert gq.gq_scale_bytes_bound(ch, 4, 768, 2048) == 4 * 2048 * 6
+    assert gq.gq_scale_bytes_bound(mx, 1, 128, 100) == 0          # cols % 128
+    assert gq.gq_scale_bytes_bound(mx, 0, 128, 128) == 0          # no groups
+    assert gq.gq_scale_bytes_bound(gq.Recipe(7, 1, 1, 0.0), 1, 128, 128) == 0
+
+
+def _desc(G, R, Ccols, kind=0, row=1, col=1):
+    d = gq.Quantized()
+    d.num_groups, d.rows_cap, d.cols = G, R, Ccols
+    d.recipe = gq.Recipe(kind, row, col, 0.0)
+    return d
+
+
+def test_quantize_host_checks_need_no_gpu(lib):
+    """Each call fails a host check, so no pointer is dereferenced and
+    nothing is launched (pointers below are never touched)."""
+    fake = C.c_void_p(0x10000)
+    st = C.c_void_p(0x20000)
+    mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    d = _desc(2, 256, 256)
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(mx), C.byref(d), None, None) == -1  # no status
+    assert lib.gq_quantize(fake, 256, 200, None, 2, C.byref(mx), C.byref(d), st, None) == -2    # cols % 128
+    assert lib.gq_quantize(fake, 255, 256, None, 2, C.byref(mx), C.byref(d), st, None) == -2    # R % G
+    assert lib.gq_quantize(fake, 256, 256, None, 0, C.byref(mx), C.byref(d), st, None) == -1    # G = 0
+    assert lib.gq_quantize(fake, 256, 256, None, 2000, C.byref(mx), C.byref(d), st, None) == -1  # G > 1024
+    assert lib.gq_quantize(fake, 256, 256, None, 4, C.byref(mx), C.byref(d), st, None) == -7    # descriptor G
+    d2 = _desc(2, 256, 256)                                                                     # no buffers
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(mx), C.byref(d2), st, None) == -1
+    d3 = _desc(2, 256, 256, kind=1, row=0, col=1)
+    ch_row = gq.Recipe(gq.RECIPE_CHANNEL128_F32, 1, 1, 1e-30)
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(ch_row), C.byref(d3), st, None) == -4
+    odd = C.c_void_p(0x10008)                                                                   # not 16B aligned
+    assert lib.gq_quantize(odd, 256, 256, None, 2, C.byref(mx), C.byref(d), st, None) == -2
+
+
+def test_gemm_host_checks_need_no_gpu(lib):
+    st = C.c_void_p(0x20000)
+    out = C.c_void_p(0x30000)
+    x = _desc(1, 256, 256, row=1, col=0)
+    x.row_data, x.row_scale, x.row_scale_bytes = 0x40000, 0x50000, 1 << 20
+    w = _desc(1, 128, 256, row=1, col=0)
+    w.row_data, w.row_scale, w.row_scale_bytes = 0x60000, 0x70000, 1 << 20
+    # k disagrees with the descriptors
+    assert lib.gq_gemm_fprop(C.byref(x), C.byref(w), None, 1, 128, 384, out, 0, st, None) == -7
+    # n not a multiple of 128
+    assert lib.gq_gemm_fprop(C.byref(x), C.byref(w), None, 1, 96, 256, out, 0, st, None) == -2
+    # bad output dtype
+    assert lib.gq_gemm_fprop(C.byref(x), C.byref(w), None, 1, 128, 256, out, 9, st, None) == -4
+    # dgrad needs the weight columnwise
+    dy = _desc(1, 256, 128, row=1, col=0)
+    dy.row_data, dy.row_scale, dy.row_scale_bytes = 0x40000, 0x50000, 1 << 20
+    assert lib.gq_gemm_dgrad(C.byref(dy), C.byref(w), None, 1, 128, 256, out, 0, st, None) in (-4, -7)
+    # wgrad needs columnwise operands, same recipe, accumulate in {0, 1}
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 0, st, None) in (-4, -7)
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 2, st, None) == -1
+    xc = _desc(1, 256, 256, kind=1, row=0, col=1)
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(xc), None, 1, 128, 256, out, 0, st, None) == -4
+    # scale capacity below the bound
+    x2 = _desc(1, 256, 256, row=1, col=0)
+    x2.row_data, x2.row_scale, x2.row_scale_bytes = 0x40000, 0x50000, 16
+    assert lib.gq_gemm_fprop(C.byref(x2), C.byref(w), None, 1, 128, 256, out, 0, st, None) == -1
+
+
+def test_binding_refuses_host_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((128, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gq._ptr(x, "x")

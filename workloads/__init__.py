@@ -213,3 +213,38 @@ def kgrouped_zero_channel_operands(w: Workload):
             dy[off:off + m, 0] = 0
         off += int(m)
     return dy, x
+
+
+def device_normal_bf16(shape, seed: int, scale: float = 1.0, stream: int = 0, device="cuda"):
+    """N(0, scale^2) bf16 tensor drawn on the device (torch Philox generator
+    seeded by (seed, stream)); used for full-size buffers that would take too
+    long to draw on the host.  Returns a torch tensor."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(int(seed) * 1000003 + int(stream))
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.normal_(0.0, float(scale), generator=g)
+    return t.to(torch.bfloat16)
+
+
+def device_uniform_bf16(shape, seed: int, lo: float, hi: float, stream: int = 0, device="cuda"):
+    """Uniform[lo, hi) bf16 tensor drawn on the device (padding garbage)."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(int(seed) * 1000003 + 7919 + int(stream))
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.uniform_(float(lo), float(hi), generator=g)
+    return t.to(torch.bfloat16)
+
+
+def device_activation(w: Workload, cols: int, stream: int, scale: float = 1.0, device="cuda"):
+    """Device [rows_cap, cols] bf16 buffer: N(0, scale^2) live rows followed by
+    the workload's padding rows (uniform[-4, 4] garbage or a constant fill)."""
+    import torch
+    out = torch.empty((w.rows_cap, cols), dtype=torch.bfloat16, device=device)
+    L = w.live_rows
+    out[:L] = device_normal_bf16((L, cols), w.seed, scale, stream, device)
+    if w.rows_cap > L:
+        if w.pad_kind == "uniform4":
+            out[L:] = device_uniform_bf16((w.rows_cap - L, cols), w.seed, -4.0, 4.0, stream, device)
+        else:
+            out[L:] = 3.0 if w.pad_kind == "fill3" else 0.0
+    return out
