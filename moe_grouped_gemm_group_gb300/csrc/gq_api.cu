@@ -10,30 +10,6 @@
 #include "gq.h"
 #include "gq_internal.h"
 
-namespace gq {
-
-const DeviceInfo& device_info()
-{
-    static DeviceInfo infos[64];
-    static std::once_flag flags[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        dev = 0;
-    std::call_once(flags[dev], [dev] {
-        DeviceInfo& d = infos[dev];
-        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
-        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
-        int optin = 0;
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        d.smem_optin = (size_t)optin;
-        if (d.sm_count <= 0)
-            d.sm_count = 1;
-    });
-    return infos[dev];
-}
-
-}  // namespace gq
 
 namespace {
 
@@ -214,6 +190,7 @@ gq::GemmOperand operand(const gq_quantized* q, bool colwise)
     gq::GemmOperand o;
     o.data = (const uint8_t*)(colwise ? q->col_data : q->row_data);
     o.scale = colwise ? q->col_scale : q->row_scale;
+    o.scale_bytes = colwise ? q->col_scale_bytes : q->row_scale_bytes;
     o.rows = q->rows_cap;
     o.cols = q->cols;
     return o;

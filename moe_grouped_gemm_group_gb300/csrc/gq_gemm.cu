@@ -45,6 +45,13 @@ namespace gq {
 namespace {
 
 constexpr int BM = 128;     // MMA M (rows of the A side)
+// L2 prefetch distance of the producers, in k-tiles (tuning knob; 0 = off):
+// the operand boxes of k-tile kt + PF are prefetched into L2 when k-tile kt
+// is loaded, so that first-touch DRAM latency hides behind the smem ring.
+#ifndef GQ_PF_DIST
+#define GQ_PF_DIST 0
+#endif
+constexpr int PF_DIST = GQ_PF_DIST;
 constexpr int BK = 128;     // k-tile depth in elements (= bytes for e4m3)
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -60,31 +67,40 @@ struct GemmArgs {
     int32_t* status;
 };
 
-template <int BN>
+template <int KIND, int BN>
 struct MxShape {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SFA_BYTES = 512;
     static constexpr int SFB_BYTES = 512 * (BN / 128);
     static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    // wgrad stages its fp32 output tile in shared memory (TMA load of the
+    // old main grad, TMA store of the result): BN / 32 boxes of 128 x 32.
+    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? BM * BN * 4 : 0;
     static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
-    static constexpr uint32_t SFA_COL = ACC * BN;                     // TMEM column of A scales
-    static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales
+    // Scale factors rotate through SF_SLOTS column groups, so that the copy
+    // for k-tile i + 1 never overwrites columns the MMAs of k-tile i still
+    // read (one shared slot would serialise the tensor pipe every k-tile).
+    static constexpr uint32_t SF_SLOTS = 8;
+    static constexpr uint32_t SF_STRIDE = 4 + BN / 32;                // A atom + B atoms
+    static constexpr uint32_t SFA_COL = ACC * BN;                     // TMEM column of A scales, slot 0
+    static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales, slot 0
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1) + 16;
-    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - SCAN_BYTES - BAR_BYTES) / STAGE;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 5) + 16;
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - OUT_BYTES - SCAN_BYTES - BAR_BYTES) / STAGE;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + SCAN_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
-    static_assert(SFB_COL + BN / 32 <= TMEM_COLS, "TMEM budget");
+    static_assert(SFA_COL + SF_SLOTS * SF_STRIDE <= TMEM_COLS, "TMEM budget");
 };
 
 // Shared-memory carve-up common to the GEMM kernels.
 struct Carve {
     uint8_t* a;
     uint8_t* b;
+    uint8_t* out;         // output staging tile (wgrad), 1024-aligned
     uint8_t* sfa;
     uint8_t* sfb;
     uint64_t* full;
@@ -92,6 +108,7 @@ struct Carve {
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
+    uint64_t* ofull;      // [4] old output boxes landed (wgrad accumulate)
     uint32_t* tmem_base;
     volatile int* abort;
     int64_t* s_off;
@@ -101,7 +118,7 @@ struct Carve {
 };
 
 __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, int b_bytes,
-                                       int sfa_bytes, int sfb_bytes, int acc)
+                                       int sfa_bytes, int sfb_bytes, int acc, int out_bytes = 0)
 {
     Carve c;
     uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
@@ -110,6 +127,8 @@ __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, in
     p += stages * a_bytes;
     c.b = p;
     p += stages * b_bytes;
+    c.out = p;
+    p += out_bytes;
     c.sfa = p;
     p += stages * sfa_bytes;
     c.sfb = p;
@@ -120,7 +139,8 @@ __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, in
     c.tfull = c.empty + 8;
     c.tempty = c.tfull + acc;
     c.drain = c.tempty + acc;
-    c.tmem_base = reinterpret_cast<uint32_t*>(c.drain + 1);
+    c.ofull = c.drain + 1;
+    c.tmem_base = reinterpret_cast<uint32_t*>(c.ofull + 4);
     c.abort = reinterpret_cast<volatile int*>(c.tmem_base + 1);
     c.s_off = reinterpret_cast<int64_t*>(c.tmem_base + 4);
     c.s_tp = reinterpret_cast<int32_t*>(c.s_off + GQ_MAX_GROUPS + 1);
@@ -243,14 +263,14 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t 
 template <int KIND, int BN, bool OUT_BF16>
 __global__ void __launch_bounds__(256, 1)
 k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-          const GemmArgs p)
+          const __grid_constant__ CUtensorMap tma_o, const GemmArgs p)
 {
-    using S = MxShape<BN>;
+    using S = MxShape<KIND, BN>;
     constexpr bool A_MN = (KIND == GEMM_WGRAD_MX);
     constexpr bool B_MN = (KIND != GEMM_FPROP);
     extern __shared__ uint8_t smem_raw[];
     const Carve c = carve(smem_raw, S::STAGES, S::A_BYTES, S::B_BYTES, S::SFA_BYTES, S::SFB_BYTES,
-                          S::ACC);
+                          S::ACC, S::OUT_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (load_status(p.status) != 0)
@@ -272,6 +292,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::mbar_init(&c.tempty[a], 4);
         }
         ptx::mbar_init(c.drain, 1);
+        for (int i = 0; i < 4; ++i)
+            ptx::mbar_init(c.ofull + i, 1);
         *c.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -282,6 +304,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tma_a);
         ptx::prefetch_tmap(&tma_b);
+        if (KIND == GEMM_WGRAD_MX)
+            ptx::prefetch_tmap(&tma_o);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -307,6 +331,24 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 uint8_t* sb = c.b + s * S::B_BYTES;
                 uint8_t* ssfa = c.sfa + s * S::SFA_BYTES;
                 uint8_t* ssfb = c.sfb + s * S::SFB_BYTES;
+                if (PF_DIST > 0 && kt + PF_DIST < t.nk) {
+                    const int kp = kt + PF_DIST;
+                    if (KIND == GEMM_FPROP) {
+                        ptx::tma_prefetch_l2_2d(&tma_a, kp * BK, (int32_t)t.row0);
+                        ptx::tma_prefetch_l2_2d(&tma_b, kp * BK, (int32_t)(t.g * p.n + t.col0));
+                    } else if (KIND == GEMM_DGRAD) {
+                        ptx::tma_prefetch_l2_2d(&tma_a, kp * BK, (int32_t)t.row0);
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            ptx::tma_prefetch_l2_2d(&tma_b, (int32_t)(t.col0 + 128 * j), (int32_t)(t.g * p.n + kp * BK));
+                    } else {
+                        const int32_t rp = (int32_t)(t.row0 + (int64_t)kp * BK);
+                        ptx::tma_prefetch_l2_2d(&tma_a, (int32_t)(t.mt * BM), rp);
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            ptx::tma_prefetch_l2_2d(&tma_b, (int32_t)(t.col0 + 128 * j), rp);
+                    }
+                }
                 if (KIND == GEMM_FPROP) {
                     const int64_t kb = p.k / 128;
                     ptx::tma_load_2d(sa, &tma_a, bar, kt * BK, (int32_t)t.row0);
@@ -371,11 +413,12 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                ptx::tc_cp_sf_atom(tmem + S::SFA_COL,
+                const uint32_t sf_off = (uint32_t)(consumed % S::SF_SLOTS) * S::SF_STRIDE;
+                ptx::tc_cp_sf_atom(tmem + S::SFA_COL + sf_off,
                                    ptx::smem_desc(ptx::smem_addr(c.sfa + s * S::SFA_BYTES), 0, 128, 0));
 #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)
-                    ptx::tc_cp_sf_atom(tmem + S::SFB_COL + 4 * j,
+                    ptx::tc_cp_sf_atom(tmem + S::SFB_COL + sf_off + 4 * j,
                                        ptx::smem_desc(ptx::smem_addr(c.sfb + s * S::SFB_BYTES + 512 * j),
                                                       0, 128, 0));
                 const uint32_t a_addr = ptx::smem_addr(c.a + s * S::A_BYTES);
@@ -389,7 +432,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     const uint64_t bd = B_MN ? ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2)
                                              : ptx::smem_desc(b_addr + 32 * j, 16, 1024, 2);
                     ptx::tc_mma_mxf8(d, ad, bd, ptx::idesc_mxf8(BM, BN, A_MN, B_MN, (uint32_t)j),
-                                     tmem + S::SFA_COL, tmem + S::SFB_COL, (kt | j) != 0);
+                                     tmem + S::SFA_COL + sf_off, tmem + S::SFB_COL + sf_off, (kt | j) != 0);
                 }
                 ptx::tc_commit(&c.empty[s]);
             }
@@ -401,8 +444,140 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         ptx::tc_commit(c.drain);
         volatile int no_abort = 0;
         ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
+    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
+        // ------------------------------------------- wgrad epilogue --
+        // The fp32 output tile moves through a ring of four 128-byte-swizzled
+        // shared boxes of 128 rows x 32 columns (one per 32-column slice of
+        // the accumulator).  The lead thread keeps TMA loads of the old main
+        // grad (accumulate) up to three boxes ahead, across tile boundaries;
+        // for each box the 128 epilogue threads add their TMEM row into the
+        // box and the lead TMA-stores it.  A slot is reloaded only after the
+        // store that last read it has finished reading (bulk wait_group.read).
+        const int q = warp & 3;
+        const uint32_t r = 32 * q + lane;
+        const bool lead = (warp == 4 && lane == 0);
+        constexpr int NB = BN / 32;                 // boxes per tile
+        constexpr int BOX = BM * 128;               // bytes per box
+        int64_t tiles_done = 0;
+        int64_t q_proc = 0, q_load = 0;             // boxes processed / loads issued
+        int64_t ld_tile = blockIdx.x;               // tile cursor of the load issuer
+        int ld_box = 0;
+        // Issue old-value loads until `ahead` boxes beyond q_proc are in flight.
+        auto issue_loads = [&](int64_t limit) {
+            while (q_load < limit) {
+                while (ld_tile < ntiles) {          // skip tiles without output
+                    const Tile lt = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, ld_tile);
+                    if (!lt.skip)
+                        break;
+                    ld_tile += gridDim.x;
+                }
+                if (ld_tile >= ntiles)
+                    return;
+                const Tile lt = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, ld_tile);
+                // the slot last held box q_load - 4, whose store has been committed
+                // among the q_proc groups so far: allow the newer ones to pend
+                if (q_load >= 4) {
+                    const int64_t pend = q_proc - (q_load - 4) - 1;
+                    if (pend <= 0)
+                        ptx::bulk_wait_read_all();
+                    else if (pend == 1)
+                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    else if (pend == 2)
+                        asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+                    else
+                        asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+                }
+                const int slot = (int)(q_load & 3);
+                uint64_t* ob = c.ofull + slot;
+                ptx::mbar_arrive_expect_tx(ob, BOX);
+                ptx::tma_load_2d(c.out + slot * BOX, &tma_o, ob, (int32_t)(lt.col0 + 32 * ld_box),
+                                 (int32_t)((int64_t)lt.g * p.n + lt.mt * BM));
+                ++q_load;
+                if (++ld_box == NB) {
+                    ld_box = 0;
+                    ld_tile += gridDim.x;
+                }
+            }
+        };
+        bool stop = false;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip)
+                continue;
+            const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM);
+            const int acc = (int)(tiles_done % S::ACC);
+            const uint32_t acc_ph = (uint32_t)((tiles_done / S::ACC) & 1);
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
+            bool ok = true;
+            if (t.nk > 0)
+                ok = ptx::mbar_wait(&c.tfull[acc], acc_ph, c.abort, p.status);
+            if (ok && t.nk > 0)
+                ptx::tc_fence_after_sync();
+#pragma unroll 1
+            for (int cc = 0; cc < NB; ++cc, ++q_proc) {
+                const int slot = (int)(q_proc & 3);
+                if (p.accumulate) {
+                    if (lead)
+                        issue_loads(q_proc + 4);
+                    if (ok)
+                        ok = ptx::mbar_wait(c.ofull + slot, (uint32_t)((q_proc >> 2) & 1), c.abort,
+                                            p.status);
+                } else if (lead) {
+                    // the store of box q_proc - 4 read this slot; newer ones may pend
+                    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+                }
+                if (ptx::named_barrier_or(1, 128, !ok)) {
+                    stop = true;
+                    break;
+                }
+                uint32_t v[32];
+                if (t.nk > 0) {
+                    ptx::tmem_ld_32x32(tbase + 32 * cc, v);
+                    ptx::tmem_wait_ld(v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = 0u;
+                }
+                const uint32_t box = ptx::smem_addr(c.out + slot * BOX);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = box + ptx::swz128(r, j);
+                    uint4 o = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    if (p.accumulate) {
+                        const uint4 old = ptx::lds128(addr);
+                        o.x = __float_as_uint(__uint_as_float(old.x) + __uint_as_float(o.x));
+                        o.y = __float_as_uint(__uint_as_float(old.y) + __uint_as_float(o.y));
+                        o.z = __float_as_uint(__uint_as_float(old.z) + __uint_as_float(o.z));
+                        o.w = __float_as_uint(__uint_as_float(old.w) + __uint_as_float(o.w));
+                    }
+                    ptx::sts128(addr, o);
+                }
+                if (cc == NB - 1 && t.nk > 0) {
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&c.tempty[acc]);
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::named_barrier_or(1, 128, 0);
+                if (lead) {
+                    ptx::tma_store_2d(&tma_o, c.out + slot * BOX, (int32_t)(t.col0 + 32 * cc), orow);
+                    ptx::bulk_commit_group();
+                }
+            }
+            if (t.nk > 0)
+                ++tiles_done;
+        }
+        if (lead) {
+            volatile int no_abort = 0;
+            for (int64_t qq = q_proc; qq < q_load; ++qq)      // loads issued but not consumed
+                if (!ptx::mbar_wait(c.ofull + (qq & 3), (uint32_t)((qq >> 2) & 1), &no_abort, p.status))
+                    break;
+            ptx::bulk_wait_all();
+        }
     } else if (warp >= 4) {
-        // --------------------------------------------------- epilogue --
+        // ------------------------------------------ fprop/dgrad epilogue --
         const int q = warp & 3;
         const int r = 32 * q + lane;        // row of the tile this thread writes
         int64_t tiles_done = 0;
@@ -465,6 +640,280 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
 }
 
 // ------------------------------------------------------------------------ //
+// MXFP8 grouped GEMM on CTA pairs (fprop, dgrad)                            //
+// ------------------------------------------------------------------------ //
+//
+// A cluster of two CTAs computes a 256 x 256 output tile with 2-SM MMAs
+// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 32): CTA r of the pair
+// holds A rows [128 r, 128 r + 128) of the tile and B rows (output columns)
+// [128 r, 128 r + 128) in its own shared memory, the full 256-column set of
+// B scale atoms, and its 128 x 256 slice of the accumulator in its own TMEM.
+// Per k-tile each CTA moves 33 KB for 2 x 128 x 256 x 128 MACs -- half the
+// operand traffic per MAC of a 128 x 128 single-CTA tile.
+//
+// Both producers signal the leader's `full` barrier (TMA with cta_group::2);
+// the leader's single MMA thread waits on it, copies the scale atoms to both
+// TMEMs, issues the MMAs, and commits stages and finished accumulators back
+// to both CTAs (multicast commit).  Epilogue warps of both CTAs drain their
+// TMEM slice (8 warps, 128 columns each), hand the accumulator back to the
+// leader, then convert and store from registers.
+
+// Whether fprop/dgrad use CTA pairs (tuning knob).
+#ifndef GQ_PAIRS
+#define GQ_PAIRS 0
+#endif
+constexpr bool kUsePairs = GQ_PAIRS != 0;
+constexpr int P_BN = 256;          // N of the pair MMA (output columns per tile)
+constexpr int P_STAGE = 16384 + 16384 + 512 + 1024;   // A half, B half, SFA atom, 2 SFB atoms
+constexpr int P_STAGES = 6;
+constexpr int P_SCAN = (GQ_MAX_GROUPS + 1) * 8 + 2 * (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 64 * 4;
+constexpr int P_BAR = 8 * (2 * P_STAGES + 3) + 16;
+constexpr int P_SMEM = 1024 + P_STAGES * P_STAGE + P_BAR + P_SCAN;
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_THREADS = 128 + 32 * P_EPI_WARPS;
+constexpr uint32_t P_TMEM_COLS = 512;
+constexpr uint32_t P_SFA_COL = P_BN;          // accumulator in columns [0, 256)
+constexpr uint32_t P_SFB_COL = P_BN + 4;
+constexpr uint32_t P_SF_SLOTS = 8;            // rotating scale-factor column groups
+constexpr uint32_t P_SF_STRIDE = 12;          // A atom (4 columns) + 2 B atoms (8 columns)
+static_assert(P_SFA_COL + P_SF_SLOTS * P_SF_STRIDE <= P_TMEM_COLS, "TMEM budget");
+static_assert(P_SMEM <= kSmemLimit, "shared memory budget");
+
+struct PairArgs {
+    GemmArgs g;
+    int64_t sfa_rows;     // rows (of 256 bytes) of the scale maps
+    int64_t sfb_rows;
+};
+
+template <int KIND, bool OUT_BF16>
+__global__ void __launch_bounds__(P_THREADS, 1)
+k_gemm_mx2(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+           const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
+           const GemmArgs p)
+{
+    constexpr bool B_MN = (KIND == GEMM_DGRAD);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = base;
+    uint8_t* sB = sA + P_STAGES * 16384;
+    uint8_t* sSFA = sB + P_STAGES * 16384;
+    uint8_t* sSFB = sSFA + P_STAGES * 512;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + P_STAGES * 1024);
+    uint64_t* empty = full + P_STAGES;
+    uint64_t* tfull = empty + P_STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int64_t* s_off = reinterpret_cast<int64_t*>(tmem_slot + 4);
+    int32_t* s_tp = reinterpret_cast<int32_t*>(s_off + GQ_MAX_GROUPS + 1);
+    int32_t* s_tq = s_tp + GQ_MAX_GROUPS + 2;
+    int64_t* s_w64 = reinterpret_cast<int64_t*>(s_tq + GQ_MAX_GROUPS + 2);
+    int32_t* s_w32 = reinterpret_cast<int32_t*>(s_w64 + 32);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_rank();
+    const bool leader = rank == 0;
+    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    // The status word is read once per CTA before any cluster-wide step; both
+    // CTAs of a pair see the same value unless it changes in between, in
+    // which case both still reach every cluster barrier below.
+    const bool noop = load_status(p.status) != 0;
+    const int err = noop ? 0 : block_scan_splits(p.splits, p.G, p.rows_cap, 32, s_off, s_tp,
+                                                 s_w64, s_w32, s_tq);
+    if (!noop && err && threadIdx.x == 0 && leader)
+        set_status(p.status, err);
+    const bool work = !noop && !err;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            ptx::mbar_init(&full[s], 2);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 2 * P_EPI_WARPS);
+        ptx::mbar_init(drain, 1);
+        *abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tma_a);
+        ptx::prefetch_tmap(&tma_b);
+        ptx::prefetch_tmap(&tma_sfa);
+        ptx::prefetch_tmap(&tma_sfb);
+    }
+    ptx::tc_fence_before_sync();
+    ptx::cluster_sync();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t nnt = (KIND == GEMM_FPROP ? p.n : p.k) / P_BN;
+    const int64_t ntiles = work ? (int64_t)s_tq[p.G] * nnt : 0;
+    const int nk = (int)((KIND == GEMM_FPROP ? p.k : p.n) / BK);
+    const int64_t kb = nk;                                   // 128-deep k-tiles = scale atoms per row tile
+    const uint32_t full0 = ptx::map_to_cta(ptx::smem_addr(&full[0]), 0);
+    const uint32_t tempty0 = ptx::map_to_cta(ptx::smem_addr(tempty), 0);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer --
+        int64_t issued = 0;
+        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
+            const int64_t rt = tile / nnt, nt = tile - rt * nnt;
+            const int g = group_of_tile(s_tq, p.G, rt);
+            const int64_t mt128 = 2 * (rt - s_tq[g]) + rank;        // this CTA's 128-row tile
+            const int32_t row0 = (int32_t)(s_off[g] + 128 * mt128);
+            const int64_t col0 = nt * P_BN;
+            bool ok = true;
+            for (int kt = 0; kt < nk; ++kt, ++issued) {
+                const int s = (int)(issued % P_STAGES);
+                const uint32_t ph = (uint32_t)((issued / P_STAGES) & 1);
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bar = full0 + 8u * s;
+                if (PF_DIST > 0 && kt + PF_DIST < nk) {
+                    const int kp = kt + PF_DIST;
+                    ptx::tma_prefetch_l2_2d(&tma_a, kp * BK, row0);
+                    if (KIND == GEMM_FPROP)
+                        ptx::tma_prefetch_l2_2d(&tma_b, kp * BK, (int32_t)(g * p.n + col0 + 128 * rank));
+                    else
+                        ptx::tma_prefetch_l2_2d(&tma_b, (int32_t)(col0 + 128 * rank), (int32_t)(g * p.n + kp * BK));
+                }
+                ptx::mbar_arrive_expect_tx_cluster(bar, P_STAGE);
+                ptx::tma_load_2d_pair(sA + s * 16384, &tma_a, bar, kt * BK, row0);
+                // scale atoms as rows of 256 bytes: atom a = rows 2a, 2a + 1
+                if (KIND == GEMM_FPROP) {
+                    ptx::tma_load_2d_pair(sB + s * 16384, &tma_b, bar, kt * BK,
+                                          (int32_t)(g * p.n + col0 + 128 * rank));
+                    ptx::tma_load_2d_pair(sSFA + s * 512, &tma_sfa, bar, 0,
+                                          (int32_t)(2 * (kb * s_tp[g] + mt128 * kb + kt)));
+                    const int64_t wbase = kb * (int64_t)g * (p.n / 128);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        ptx::tma_load_2d_pair(sSFB + s * 1024 + 512 * j, &tma_sfb, bar, 0,
+                                              (int32_t)(2 * (wbase + (col0 / 128 + j) * kb + kt)));
+                } else {
+                    const int64_t nb = p.n / 128;
+                    ptx::tma_load_2d_pair(sB + s * 16384, &tma_b, bar, (int32_t)(col0 + 128 * rank),
+                                          (int32_t)(g * p.n + kt * BK));
+                    ptx::tma_load_2d_pair(sSFA + s * 512, &tma_sfa, bar, 0,
+                                          (int32_t)(2 * (nb * s_tp[g] + mt128 * nb + kt)));
+                    const int64_t wbase = (p.k / 128) * (int64_t)g * nb;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        ptx::tma_load_2d_pair(sSFB + s * 1024 + 512 * j, &tma_sfb, bar, 0,
+                                              (int32_t)(2 * (wbase + (col0 / 128 + j) * nb + kt)));
+                }
+            }
+            if (!ok)
+                break;
+        }
+        if (leader) {
+            volatile int no_abort = 0;
+            for (int64_t q = issued - P_STAGES < 0 ? 0 : issued - P_STAGES; q < issued; ++q)
+                if (!ptx::mbar_wait(&full[q % P_STAGES], (uint32_t)((q / P_STAGES) & 1), &no_abort, p.status))
+                    break;
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------------------------------- MMA issuer (leader) --
+        int64_t consumed = 0, tiles_done = 0;
+        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
+            if (!ptx::mbar_wait(tempty, (uint32_t)((tiles_done & 1) ^ 1), abort, p.status))
+                break;
+            ptx::tc_fence_after_sync();
+            bool ok = true;
+            for (int kt = 0; kt < nk; ++kt, ++consumed) {
+                const int s = (int)(consumed % P_STAGES);
+                const uint32_t ph = (uint32_t)((consumed / P_STAGES) & 1);
+                if (!ptx::mbar_wait(&full[s], ph, abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t sf_off = (uint32_t)(consumed % P_SF_SLOTS) * P_SF_STRIDE;
+                ptx::tc_cp_sf_atom_pair(tmem + P_SFA_COL + sf_off,
+                                        ptx::smem_desc(ptx::smem_addr(sSFA + s * 512), 0, 128, 0));
+                ptx::tc_cp_sf_atom_pair(tmem + P_SFB_COL + sf_off,
+                                        ptx::smem_desc(ptx::smem_addr(sSFB + s * 1024), 0, 128, 0));
+                ptx::tc_cp_sf_atom_pair(tmem + P_SFB_COL + sf_off + 4,
+                                        ptx::smem_desc(ptx::smem_addr(sSFB + s * 1024 + 512), 0, 128, 0));
+                const uint32_t a_addr = ptx::smem_addr(sA + s * 16384);
+                const uint32_t b_addr = ptx::smem_addr(sB + s * 16384);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint64_t ad = ptx::smem_desc(a_addr + 32 * j, 16, 1024, 2);
+                    const uint64_t bd = B_MN ? ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2)
+                                             : ptx::smem_desc(b_addr + 32 * j, 16, 1024, 2);
+                    ptx::tc_mma_mxf8_pair(tmem, ad, bd, ptx::idesc_mxf8(256, P_BN, 0, B_MN, (uint32_t)j),
+                                          tmem + P_SFA_COL + sf_off, tmem + P_SFB_COL + sf_off, (kt | j) != 0);
+                }
+                ptx::tc_commit_pair(&empty[s], 0x3);
+            }
+            if (!ok)
+                break;
+            ptx::tc_commit_pair(tfull, 0x3);
+            ++tiles_done;
+        }
+        ptx::tc_commit_pair(drain, 0x1);
+        volatile int no_abort = 0;
+        ptx::mbar_wait(drain, 0, &no_abort, p.status);
+    } else if (warp >= 4) {
+        // --------------------------------------------------- epilogue --
+        const int q = warp & 3, h = (warp - 4) >> 2;            // lane quadrant, column half
+        const int r = 32 * q + lane;                             // row of this CTA's slice
+        int64_t tiles_done = 0;
+        const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
+        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
+            const int64_t rt = tile / nnt, nt = tile - rt * nnt;
+            const int g = group_of_tile(s_tq, p.G, rt);
+            const int64_t m = s_off[g + 1] - s_off[g];
+            const int64_t lr = 256 * (rt - s_tq[g]) + 128 * rank + r;   // row inside the group
+            const bool live = lr < m;
+            if (!ptx::mbar_wait(tfull, (uint32_t)(tiles_done & 1), abort, p.status))
+                break;
+            ptx::tc_fence_after_sync();
+            uint32_t v[4][32];
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld_32x32(tb + 32 * c, v[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_wait_ld(v[c]);
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive_cluster(tempty0);
+            ++tiles_done;
+            if (live) {
+                const int64_t off = (s_off[g] + lr) * ld + nt * P_BN + 128 * h;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (OUT_BF16)
+                        store_row_bf16(static_cast<uint16_t*>(p.out) + off + 32 * c, v[c]);
+                    else
+                        store_row_f32(static_cast<float*>(p.out) + off + 32 * c, v[c]);
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc_pair(tmem, P_TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------ //
 // Per-channel 128-row fp32-scale k-grouped wgrad                            //
 // ------------------------------------------------------------------------ //
 //
@@ -483,8 +932,8 @@ struct ChShape {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int PBUF = 2;
     static constexpr uint32_t TMEM_COLS = 256;
-    static constexpr int SCAN_BYTES = MxShape<128>::SCAN_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * PBUF + 1) + 16;
+    static constexpr int SCAN_BYTES = MxShape<GEMM_FPROP, 128>::SCAN_BYTES;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * PBUF + 5) + 16;
     static constexpr int STAGES = 6;
     static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + SCAN_BYTES;
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
@@ -682,39 +1131,6 @@ __global__ void k_zero_fill(float* __restrict__ out, int64_t count, const int32_
 // Host side                                                                 //
 // ------------------------------------------------------------------------ //
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// 2-D map over a row-major uint8 [rows, cols] buffer with boxes of 128
-// columns x box_rows rows and 128-byte swizzle; out-of-range rows read 0.
-bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t cols, int box_rows)
-{
-    auto enc = tensor_map_encoder();
-    if (!enc)
-        return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols};
-    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <typename Kernel>
 cudaError_t prepare(Kernel kernel, int smem)
 {
@@ -722,16 +1138,56 @@ cudaError_t prepare(Kernel kernel, int smem)
 }
 
 template <int KIND, int BN, bool OUT_BF16>
-gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
-                 int64_t tiles_bound, cudaStream_t stream)
+gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                 const GemmArgs& args, int64_t tiles_bound, cudaStream_t stream)
 {
-    using S = MxShape<BN>;
+    using S = MxShape<KIND, BN>;
     auto kernel = k_gemm_mx<KIND, BN, OUT_BF16>;
     if (prepare(kernel, S::SMEM) != cudaSuccess)
         return GQ_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
-    kernel<<<(unsigned)grid, 256, S::SMEM, stream>>>(ma, mb, args);
+    kernel<<<(unsigned)grid, 256, S::SMEM, stream>>>(ma, mb, mo, args);
     return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+}
+
+template <int KIND, bool OUT_BF16>
+gq_status run_mx2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                  const CUtensorMap& msb, const GemmArgs& args, int64_t pair_tiles_bound,
+                  cudaStream_t stream)
+{
+    auto kernel = k_gemm_mx2<KIND, OUT_BF16>;
+    if (prepare(kernel, P_SMEM) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_bound, device_info().sm_count / 2));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(P_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, ma, mb, msa, msb, args) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+}
+
+// Bytes of an MX scale buffer for G groups over `rows` rows (the ABI bound).
+uint64_t mx_scale_bytes(int G, int64_t rows, int64_t cols)
+{
+    return 512ull * (uint64_t)(cols / 128) * (uint64_t)((rows + 127) / 128 + G);
+}
+
+// Scale buffer of `bytes` bytes viewed as rows of 256 bytes (an atom is two
+// rows), so that scale atoms travel by TMA with the pair's barrier.
+bool make_scale_map(CUtensorMap* map, const void* base, uint64_t bytes)
+{
+    return make_tensor_map_2d_plain(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base,
+                                    (int64_t)(bytes / 256), 256, 256, 2);
 }
 
 }  // namespace
@@ -764,28 +1220,43 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
     }
     CUtensorMap ma, mb;
     switch (kind) {
-    case GEMM_FPROP: {
-        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
-            return GQ_ERR_CUDA;
-        const int64_t bound = ((rows_cap + 127) / 128 + G) * (n / 128);
-        return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_FPROP, 128, true>(ma, mb, args, bound, stream)
-                                          : run_mx<GEMM_FPROP, 128, false>(ma, mb, args, bound, stream);
-    }
+    case GEMM_FPROP:
     case GEMM_DGRAD: {
-        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+        const int64_t n_out = kind == GEMM_FPROP ? n : k;
+        if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
-        const int64_t bound = ((rows_cap + 127) / 128 + G) * (k / 128);
-        return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_DGRAD, 128, true>(ma, mb, args, bound, stream)
-                                          : run_mx<GEMM_DGRAD, 128, false>(ma, mb, args, bound, stream);
+        if (kUsePairs && n_out % P_BN == 0 && device_info().sm_count >= 2) {
+            // CTA pairs on 256 x 256 tiles; scale atoms by TMA (rows of 256 bytes)
+            CUtensorMap msa, msb;
+            const uint64_t sa = std::min<uint64_t>(a.scale_bytes, mx_scale_bytes(G, a.rows, a.cols));
+            const uint64_t sb = std::min<uint64_t>(b.scale_bytes, mx_scale_bytes(G, b.rows, b.cols));
+            if (!make_scale_map(&msa, a.scale, sa) || !make_scale_map(&msb, b.scale, sb))
+                return GQ_ERR_CUDA;
+            const int64_t bound = ((rows_cap + 255) / 256 + G) * (n_out / P_BN);
+            if (kind == GEMM_FPROP)
+                return out_dtype == GQ_DTYPE_BF16 ? run_mx2<GEMM_FPROP, true>(ma, mb, msa, msb, args, bound, stream)
+                                                  : run_mx2<GEMM_FPROP, false>(ma, mb, msa, msb, args, bound, stream);
+            return out_dtype == GQ_DTYPE_BF16 ? run_mx2<GEMM_DGRAD, true>(ma, mb, msa, msb, args, bound, stream)
+                                              : run_mx2<GEMM_DGRAD, false>(ma, mb, msa, msb, args, bound, stream);
+        }
+        const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 128);
+        if (kind == GEMM_FPROP)
+            return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_FPROP, 128, true>(ma, mb, ma, args, bound, stream)
+                                              : run_mx<GEMM_FPROP, 128, false>(ma, mb, ma, args, bound, stream);
+        return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_DGRAD, 128, true>(ma, mb, ma, args, bound, stream)
+                                          : run_mx<GEMM_DGRAD, 128, false>(ma, mb, ma, args, bound, stream);
     }
     case GEMM_WGRAD_MX: {
-        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+        if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
+            return GQ_ERR_CUDA;
+        CUtensorMap mo;
+        if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, 128))
             return GQ_ERR_CUDA;
         const int64_t bound = (int64_t)G * (n / 128) * (k / 128);
-        return run_mx<GEMM_WGRAD_MX, 128, false>(ma, mb, args, bound, stream);
+        return run_mx<GEMM_WGRAD_MX, 128, false>(ma, mb, mo, args, bound, stream);
     }
     case GEMM_WGRAD_CHANNEL: {
-        if (!make_map(&ma, a.data, a.rows, a.cols, 128) || !make_map(&mb, b.data, b.rows, b.cols, 128))
+        if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
         if (prepare(k_gemm_wgrad_channel, ChShape::SMEM) != cudaSuccess)
             return GQ_ERR_CUDA;

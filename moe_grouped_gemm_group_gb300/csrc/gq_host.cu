@@ -1,0 +1,89 @@
+// Host-side helpers: per-device facts and the TMA tensor-map encoder (taken
+// from the driver at run time, so that loading the library needs no GPU).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gq_internal.h"
+
+namespace gq {
+
+const DeviceInfo& device_info()
+{
+    static DeviceInfo infos[64];
+    static std::once_flag flags[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        dev = 0;
+    std::call_once(flags[dev], [dev] {
+        DeviceInfo& d = infos[dev];
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        d.smem_optin = (size_t)optin;
+        if (d.sm_count <= 0)
+            d.sm_count = 1;
+    });
+    return infos[dev];
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+}  // namespace
+
+namespace {
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+               int64_t rows, int64_t cols, int box_cols, int box_rows, CUtensorMapSwizzle swizzle)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc || rows <= 0 || cols <= 0)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * (cuuint64_t)elem_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                        const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows)
+{
+    return encode_2d(map, dtype, elem_bytes, base, rows, cols, box_cols, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_tensor_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                              const void* base, int64_t rows, int64_t cols, int box_cols,
+                              int box_rows)
+{
+    return encode_2d(map, dtype, elem_bytes, base, rows, cols, box_cols, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace gq

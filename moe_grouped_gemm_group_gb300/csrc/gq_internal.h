@@ -1,6 +1,7 @@
 // Host-side declarations shared by the C-ABI layer and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -19,6 +20,25 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();
 
+// 2-D tensor map over a row-major [rows, cols] buffer of `elem_bytes`-byte
+// elements (rows stride = cols * elem_bytes), boxes of box_cols x box_rows
+// with the 128-byte swizzle; out-of-range elements read as zero.  False if
+// the driver's encoder is unavailable or rejects the map.
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                        const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows);
+
+// The same without swizzle (boxes land row after row in shared memory).
+bool make_tensor_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                              const void* base, int64_t rows, int64_t cols, int box_cols,
+                              int box_rows);
+
+inline bool make_map_u8(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t cols,
+                        int box_rows)
+{
+    return make_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, 128,
+                              box_rows);
+}
+
 // Quantizer launchers (gq_quant.cu).
 cudaError_t launch_split_scan(const int32_t* splits, int G, int64_t rows_cap, int64_t cols,
                               int align, int scale_kind, int64_t* table, int32_t* status,
@@ -35,6 +55,7 @@ cudaError_t launch_quant_channel(const void* x, int64_t rows_cap, int64_t cols,
 struct GemmOperand {
     const uint8_t* data;   // e4m3 codes [rows, cols]
     const void* scale;     // E8M0 swizzled bytes or fp32 per-channel scales
+    uint64_t scale_bytes;  // capacity of `scale` (at least the bound for its shape)
     int64_t rows;          // rows of the buffer (rows_cap, or G * n for weights)
     int64_t cols;
 };

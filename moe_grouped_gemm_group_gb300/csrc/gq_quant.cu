@@ -24,6 +24,7 @@
 
 #include "gq_device.cuh"
 #include "gq_internal.h"
+#include "gq_ptx.cuh"
 
 namespace gq {
 namespace {
@@ -109,19 +110,42 @@ __global__ void k_split_scan(const int32_t* __restrict__ splits, int G, int64_t 
     }
 }
 
+// Shared-memory plan of k_quant_mx: a ring of kQStages input tiles, each a
+// 128-row x 128-column bf16 tile loaded by TMA as two 128-byte-swizzled boxes
+// of [128 rows][64 columns]; barriers; the split scan.
+// Ring depth and CTAs per SM (tuning knobs; the defaults are the measured best).
+#ifndef GQ_Q_STAGES
+#define GQ_Q_STAGES 4
+#endif
+#ifndef GQ_Q_MINB
+#define GQ_Q_MINB 1
+#endif
+constexpr int kQStages = GQ_Q_STAGES;
+constexpr int kQTile = 128 * 128 * 2;
+constexpr int kQConsumers = 512;                       // 16 consumer warps
+constexpr int kQThreadsMx = kQConsumers + 32;          // + 1 producer warp
+constexpr int kQScanBytes = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
+constexpr int kQSmem = 1024 + kQStages * kQTile + 16 * 32 * 4 + 8 * 2 * kQStages + 16 + kQScanBytes;
+
 template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kQuantThreads, 2)
-k_quant_mx(const uint16_t* __restrict__ x, int64_t rows_cap, int64_t cols,
+__global__ void __launch_bounds__(kQThreadsMx, GQ_Q_MINB)
+k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t cols,
            const int32_t* __restrict__ splits, int G, uint8_t* __restrict__ row_data,
            uint8_t* __restrict__ row_scale, uint8_t* __restrict__ col_data,
            uint8_t* __restrict__ col_scale, int32_t* __restrict__ status)
 {
-    __shared__ int64_t s_off[GQ_MAX_GROUPS + 1];
-    __shared__ int32_t s_tp[GQ_MAX_GROUPS + 1];
-    __shared__ int64_t s_w64[32];
-    __shared__ int32_t s_w32[32];
-    __shared__ __align__(16) uint8_t s_rs[512];
-    __shared__ __align__(16) uint8_t s_cs[512];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* tiles = base;
+    float* s_inv = reinterpret_cast<float*>(tiles + kQStages * kQTile);  // [16 warps][32] column 2^-e
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_inv + 16 * 32);
+    uint64_t* empty = full + kQStages;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + kQStages);
+    int64_t* s_off = reinterpret_cast<int64_t*>(empty + kQStages + 2);
+    int32_t* s_tp = reinterpret_cast<int32_t*>(s_off + GQ_MAX_GROUPS + 1);
+    int64_t* s_w64 = reinterpret_cast<int64_t*>(s_tp + GQ_MAX_GROUPS + 2);
+    int32_t* s_w32 = reinterpret_cast<int32_t*>(s_w64 + 32);
 
     if (load_status(status) != 0)
         return;
@@ -131,13 +155,54 @@ k_quant_mx(const uint16_t* __restrict__ x, int64_t rows_cap, int64_t cols,
             set_status(status, err);
         return;
     }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kQConsumers / 32);
+        }
+        *abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
 
     const int nct = (int)(cols >> 7);
     const int64_t total = (int64_t)s_tp[G] * nct;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = warp >> 2, cb = warp & 3;
 
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    if (warp == kQConsumers / 32) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tma_x);
+            int64_t it = 0;
+            for (int64_t t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++it) {
+                const int s = (int)(it % kQStages);
+                const uint32_t ph = (uint32_t)((it / kQStages) & 1);
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort, status))
+                    break;
+                const int64_t rt = t / nct;
+                const int ct = (int)(t - rt * nct);
+                const int g = group_of_tile(s_tp, G, rt);
+                const int32_t row0 = (int32_t)(s_off[g] + 128 * (rt - s_tp[g]));
+                ptx::mbar_arrive_expect_tx(&full[s], kQTile);
+                ptx::tma_load_2d(tiles + s * kQTile, &tma_x, &full[s], ct * 128, row0);
+                ptx::tma_load_2d(tiles + s * kQTile + kQTile / 2, &tma_x, &full[s], ct * 128 + 64, row0);
+            }
+            // every issued load lands before the CTA leaves
+            volatile int no_abort = 0;
+            for (int64_t q = it - kQStages < 0 ? 0 : it - kQStages; q < it; ++q)
+                if (!ptx::mbar_wait(&full[q % kQStages], (uint32_t)((q / kQStages) & 1), &no_abort, status))
+                    break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers --
+    const int rb = warp >> 2, cb = warp & 3;
+    const uint32_t r_in_tile = 32 * rb + lane;
+    int64_t it = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        const int s = (int)(it % kQStages);
+        const uint32_t ph = (uint32_t)((it / kQStages) & 1);
         const int64_t rt = t / nct;
         const int ct = (int)(t - rt * nct);
         const int g = group_of_tile(s_tp, G, rt);
@@ -145,67 +210,119 @@ k_quant_mx(const uint16_t* __restrict__ x, int64_t rows_cap, int64_t cols,
         const int64_t m = s_off[g + 1] - s_off[g];
         const int64_t rows_here = min((int64_t)128, m - 128 * lt);   // a multiple of 32
         const bool active = 32 * rb < rows_here;                     // uniform per warp
-        const int64_t row = s_off[g] + 128 * lt + 32 * rb + lane;
+        const int64_t row = s_off[g] + 128 * lt + r_in_tile;
         const int64_t col0 = (int64_t)ct * 128 + 32 * cb;
 
-        uint32_t rbyte = 0, cbyte = 0;
-        if (active) {
-            uint32_t v[16];
-            load_row32(x + row * cols + col0, v);
-            if (ROW) {
-                uint32_t mx = 0;
+        const bool ok = ptx::mbar_wait(&full[s], ph, abort, status);
+        uint32_t v[16];
+        if (ok) {
+            // row r_in_tile, columns 32 cb .. 32 cb + 31: box cb / 2, chunks 4 (cb % 2) + i
+            const uint32_t box = ptx::smem_addr(tiles + s * kQTile + (cb >> 1) * (kQTile / 2));
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    mx = __vmaxu2(mx, v[i] & 0x7fff7fffu);
+            for (int i = 0; i < 4; ++i) {
+                const uint4 u = ptx::lds128(box + ptx::swz128(r_in_tile, 4 * (cb & 1) + i));
+                v[4 * i + 0] = u.x;
+                v[4 * i + 1] = u.y;
+                v[4 * i + 2] = u.z;
+                v[4 * i + 3] = u.w;
+            }
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&empty[s]);
+        }
+        uint32_t rbyte = 0, cbyte = 0;
+        if (ok && active) {
+            // magnitudes (sign bits cleared), two bf16 per register
+            uint32_t mg[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                mg[i] = v[i] & 0x7fff7fffu;
+            float xf[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                xf[2 * i] = bf16_lo(v[i]);
+                xf[2 * i + 1] = bf16_hi(v[i]);
+            }
+            if (ROW) {
+                uint32_t mx = mg[0];
+#pragma unroll
+                for (int i = 1; i < 16; ++i)
+                    mx = __vmaxu2(mx, mg[i]);
                 rbyte = e8m0_byte(max(mx & 0xffffu, mx >> 16));
-                const float s = inv_scale(rbyte);
+                const float sc = inv_scale(rbyte);
                 uint32_t w[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t p0 = cvt_e4m3x2(bf16_lo(v[2 * i]) * s, bf16_hi(v[2 * i]) * s);
-                    const uint32_t p1 =
-                        cvt_e4m3x2(bf16_lo(v[2 * i + 1]) * s, bf16_hi(v[2 * i + 1]) * s);
-                    w[i] = p0 | (p1 << 16);
-                }
+                for (int i = 0; i < 8; ++i)
+                    w[i] = cvt_e4m3x2(xf[4 * i] * sc, xf[4 * i + 1] * sc) |
+                           (cvt_e4m3x2(xf[4 * i + 2] * sc, xf[4 * i + 3] * sc) << 16);
                 store32(row_data + row * cols + col0, w);
             }
             if (COL) {
-                float sc[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const uint32_t am = __reduce_max_sync(0xffffffffu, mag(v, j));
-                    const uint32_t byte = e8m0_byte(am);
-                    if (lane == j)
-                        cbyte = byte;
-                    sc[j] = elem(v, j) * inv_scale(byte);
-                }
-                uint32_t w[8];
+                // Transpose-max across the warp: after exchanging half of the
+                // remaining columns with lane ^ 16, ^ 8, ^ 4, ^ 2, ^ 1, lane j
+                // holds the max over the 32 rows of column j.
+                uint32_t red[8];
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t p0 = cvt_e4m3x2(sc[4 * i + 0], sc[4 * i + 1]);
-                    const uint32_t p1 = cvt_e4m3x2(sc[4 * i + 2], sc[4 * i + 3]);
-                    w[i] = p0 | (p1 << 16);
+                    const uint32_t send = b4 ? mg[i] : mg[i + 8];
+                    const uint32_t keep = b4 ? mg[i + 8] : mg[i];
+                    red[i] = __vmaxu2(keep, __shfl_xor_sync(0xffffffffu, send, 16));
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t send = b3 ? red[i] : red[i + 4];
+                    const uint32_t keep = b3 ? red[i + 4] : red[i];
+                    red[i] = __vmaxu2(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t send = b2 ? red[i] : red[i + 2];
+                    const uint32_t keep = b2 ? red[i + 2] : red[i];
+                    red[i] = __vmaxu2(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+                }
+                {
+                    const uint32_t send = b1 ? red[0] : red[1];
+                    const uint32_t keep = b1 ? red[1] : red[0];
+                    red[0] = __vmaxu2(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+                }
+                const uint32_t pairmax = __vmaxu2(red[0], __shfl_xor_sync(0xffffffffu, red[0], 1));
+                cbyte = e8m0_byte(b0 ? (pairmax >> 16) : (pairmax & 0xffffu));
+                // broadcast the 32 column scales through shared memory
+                float* inv = s_inv + warp * 32;
+                inv[lane] = inv_scale(cbyte);
+                __syncwarp();
+                float sc[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = reinterpret_cast<const float4*>(inv)[i];
+                    sc[4 * i] = f.x;
+                    sc[4 * i + 1] = f.y;
+                    sc[4 * i + 2] = f.z;
+                    sc[4 * i + 3] = f.w;
+                }
+                __syncwarp();
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    w[i] = cvt_e4m3x2(xf[4 * i] * sc[4 * i], xf[4 * i + 1] * sc[4 * i + 1]) |
+                           (cvt_e4m3x2(xf[4 * i + 2] * sc[4 * i + 2], xf[4 * i + 3] * sc[4 * i + 3]) << 16);
                 store32(col_data + row * cols + col0, w);
             }
         }
-        // Scale atoms: rowwise (row 32 rb + lane, block cb); columnwise
-        // (channel 32 cb + lane, 32-row block rb).  Inactive warps write the
-        // zero entries of a partial last tile.
-        s_rs[lane * 16 + rb * 4 + cb] = (uint8_t)rbyte;
-        s_cs[lane * 16 + cb * 4 + rb] = (uint8_t)cbyte;
-        __syncthreads();
-        const int64_t base = 512 * (int64_t)nct * s_tp[g];
-        if (ROW && threadIdx.x < 32) {
-            const uint4 a = reinterpret_cast<const uint4*>(s_rs)[threadIdx.x];
-            reinterpret_cast<uint4*>(row_scale + base + (lt * nct + ct) * 512)[threadIdx.x] = a;
-        }
-        if (COL && threadIdx.x >= 32 && threadIdx.x < 64) {
+        if (!ok)
+            break;
+        // Scale bytes go straight to their atoms: rowwise (row 32 rb + lane,
+        // block cb), columnwise (channel 32 cb + lane, 32-row block rb).
+        // Inactive warps write the zero entries of a partial last tile.  The
+        // 16 warps together cover each 512-byte atom once.
+        const int64_t sbase = 512 * (int64_t)nct * s_tp[g];
+        if (ROW)
+            row_scale[sbase + (lt * nct + ct) * 512 + lane * 16 + rb * 4 + cb] = (uint8_t)rbyte;
+        if (COL) {
             const int64_t T = s_tp[g + 1] - s_tp[g];
-            const uint4 a = reinterpret_cast<const uint4*>(s_cs)[threadIdx.x - 32];
-            reinterpret_cast<uint4*>(col_scale + base + ((int64_t)ct * T + lt) * 512)[threadIdx.x - 32] = a;
+            col_scale[sbase + ((int64_t)ct * T + lt) * 512 + lane * 16 + cb * 4 + rb] = (uint8_t)cbyte;
         }
-        __syncthreads();
     }
 }
 
@@ -301,27 +418,29 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const
                             int G, uint8_t* row_data, uint8_t* row_scale, uint8_t* col_data,
                             uint8_t* col_scale, int32_t* status, cudaStream_t stream)
 {
+    CUtensorMap map;
+    if (!make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows_cap, cols, 64, 128))
+        return cudaErrorInvalidValue;
     const int64_t tiles_bound = ((rows_cap + 127) / 128 + G) * (cols / 128);
-    const auto* xp = static_cast<const uint16_t*>(x);
     const int sms = device_info().sm_count;
-    auto grid_for = [&](const void* fn) {
-        const int64_t g = (int64_t)sms * blocks_per_sm_for(fn, kQuantThreads);
-        return (unsigned)std::max<int64_t>(1, std::min<int64_t>(g, tiles_bound));
+    auto go = [&](auto kernel) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+        if (e != cudaSuccess)
+            return e;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQThreadsMx, kQSmem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, tiles_bound));
+        kernel<<<(unsigned)grid, kQThreadsMx, kQSmem, stream>>>(map, rows_cap, cols, splits, G, row_data,
+                                                                row_scale, col_data, col_scale, status);
+        return cudaGetLastError();
     };
-    if (row_data && col_data) {
-        const void* fn = (const void*)k_quant_mx<true, true>;
-        k_quant_mx<true, true><<<grid_for(fn), kQuantThreads, 0, stream>>>(
-            xp, rows_cap, cols, splits, G, row_data, row_scale, col_data, col_scale, status);
-    } else if (row_data) {
-        const void* fn = (const void*)k_quant_mx<true, false>;
-        k_quant_mx<true, false><<<grid_for(fn), kQuantThreads, 0, stream>>>(
-            xp, rows_cap, cols, splits, G, row_data, row_scale, col_data, col_scale, status);
-    } else {
-        const void* fn = (const void*)k_quant_mx<false, true>;
-        k_quant_mx<false, true><<<grid_for(fn), kQuantThreads, 0, stream>>>(
-            xp, rows_cap, cols, splits, G, row_data, row_scale, col_data, col_scale, status);
-    }
-    return cudaGetLastError();
+    if (row_data && col_data)
+        return go(k_quant_mx<true, true>);
+    if (row_data)
+        return go(k_quant_mx<true, false>);
+    return go(k_quant_mx<false, true>);
 }
 
 cudaError_t launch_quant_channel(const void* x, int64_t rows_cap, int64_t cols,

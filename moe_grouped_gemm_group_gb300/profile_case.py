@@ -1,0 +1,106 @@
+"""Profiling driver: run one kernel of the path on a mid-size case, a few times.
+
+Meant to be run under a profiler (Nsight Compute) with a kernel filter and a
+launch count, e.g.
+
+    python -m moe_grouped_gemm_group_gb300.profile_case fprop --reps 3
+    ncu --set full --clock-control none -k regex:k_gemm_mx -s 1 -c 1 -o prof \\
+        python -m moe_grouped_gemm_group_gb300.profile_case fprop --reps 3
+
+Cases (seeded synthetic inputs; a few GB on the device at most, every input
+larger than the 129 MB L2):
+  quant       MXFP8 row+col quantisation of the moe_e64_zipf fc1 input
+              ([66560, 7168] bf16, 65536 live rows)
+  fprop       moe_e64_zipf fc1 fprop (n 2048, k 7168, bf16 output)
+  dgrad       moe_e64_zipf fc1 dgrad (bf16 output)
+  wgrad       moe_e8 fc1 k-grouped wgrad accumulating into fp32 (8 x 2048 x 4096)
+  wgrad_ch    kgrouped_zero_channel per-channel wgrad (4 x 2048 x 2048)
+Prints the mean CUDA-event time per launch.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["quant", "fprop", "dgrad", "wgrad", "wgrad_ch"])
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+
+    import numpy as np
+    import torch
+
+    import moe_grouped_gemm_group_gb300 as gq
+    import workloads as W
+
+    dev = "cuda:0"
+    gq.load()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    name = "moe_e8" if args.case == "wgrad" else "moe_e64_zipf"
+    w = W.workload(name)
+    E, H, F, R = w.num_groups, w.hidden, w.ffn, w.rows_cap
+    sp = torch.as_tensor(w.splits).to(dev)
+
+    def quant(t, splits):
+        q = gq.alloc_quantized(t.shape[0], t.shape[1], E, mx, dev)
+        gq.gq_quantize(t, splits, E, mx, q, st)
+        return q
+
+    if args.case == "quant":
+        x = W.device_activation(w, H, 0, device=dev)
+        q = gq.alloc_quantized(R, H, E, mx, dev)
+        fn = lambda: gq.gq_quantize(x, sp, E, mx, q, st)  # noqa: E731
+    elif args.case in ("fprop", "dgrad"):
+        wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
+        qw = quant(wt, None)
+        del wt
+        if args.case == "fprop":
+            qx = quant(W.device_activation(w, H, 0, device=dev), sp)
+            y = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_fprop(qx, qw, sp, E, F, H, y, gq.DTYPE_BF16, st)  # noqa: E731
+        else:
+            qd = quant(W.device_activation(w, F, 2, device=dev), sp)
+            dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, F, H, dx, gq.DTYPE_BF16, st)  # noqa: E731
+    elif args.case == "wgrad":
+        qx = quant(W.device_activation(w, H, 0, device=dev), sp)
+        qd = quant(W.device_activation(w, F, 2, device=dev), sp)
+        dw = W.device_normal_bf16((E, F, H), w.seed, 1e-3, 20, dev).float()
+        fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, True, st)  # noqa: E731
+    else:
+        cw = W.workload("kgrouped_zero_channel")
+        dyc, xc = W.kgrouped_zero_channel_operands(cw)
+        ch = gq.Recipe(gq.RECIPE_CHANNEL128_F32, 0, 1, 1e-30)
+        csp = torch.as_tensor(cw.splits).to(dev)
+        qs = {}
+        for k, b in (("dy", dyc), ("x", xc)):
+            qs[k] = gq.alloc_quantized(cw.rows_cap, b.shape[1], 4, ch, dev)
+            gq.gq_quantize(torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16), csp, 4, ch,
+                           qs[k], st)
+        dw = torch.empty((4, cw.hidden, cw.ffn), device=dev)
+        fn = lambda: gq.gq_gemm_wgrad(qs["dy"], qs["x"], csp, 4, cw.hidden, cw.ffn, dw, False, st)  # noqa: E731
+
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    ms = [a.elapsed_time(b) for a, b in evs]
+    print(f"{args.case}: {args.reps} launches, mean {np.mean(ms):.4f} ms, min {np.min(ms):.4f} ms")
+
+
+if __name__ == "__main__":
+    main()

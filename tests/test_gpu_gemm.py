@@ -116,6 +116,8 @@ CASES = [
     ([128, 384, 0, 32, 224], 32, 256, 640),
     ([0, 0, 64], 0, 128, 128),
     ([1024, 32, 736], 96, 512, 512),
+    ([32, 0, 96, 288, 160], 64, 256, 256),       # CTA-pair tiles with empty halves
+    ([2048, 224], 0, 768, 512),
 ]
 
 
