@@ -69,6 +69,10 @@ struct GemmArgs {
 
 template <int KIND, int BN>
 struct MxShape {
+    // BN = 128: 4 epilogue warps, one row per thread; BN = 256: 8 epilogue
+    // warps (two per TMEM lane quadrant, 128 columns each).
+    static constexpr int EPI_WARPS = BN == 256 ? 8 : 4;
+    static constexpr int THREADS = 128 + 32 * EPI_WARPS;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SFA_BYTES = 512;
@@ -261,7 +265,7 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t 
 // ------------------------------------------------------------------------ //
 
 template <int KIND, int BN, bool OUT_BF16>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(MxShape<KIND, BN>::THREADS, 1)
 k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
           const __grid_constant__ CUtensorMap tma_o, const GemmArgs p)
 {
@@ -289,7 +293,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         }
         for (int a = 0; a < S::ACC; ++a) {
             ptx::mbar_init(&c.tfull[a], 1);
-            ptx::mbar_init(&c.tempty[a], 4);
+            ptx::mbar_init(&c.tempty[a], S::EPI_WARPS);
         }
         ptx::mbar_init(c.drain, 1);
         for (int i = 0; i < 4; ++i)
@@ -576,7 +580,47 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     break;
             ptx::bulk_wait_all();
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && BN == 256) {
+        // ------------------------------ fprop/dgrad epilogue, 256 columns --
+        // One accumulator fills TMEM, so it is drained into registers (each
+        // of 8 warps takes its lane quadrant's 32 rows x 128 columns) and
+        // handed back before the stores; the next tile's MMAs overlap them.
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        const int r = 32 * q + lane;
+        const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
+        int64_t tiles_done = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip || t.nk == 0)
+                continue;
+            if (!ptx::mbar_wait(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
+                break;
+            ptx::tc_fence_after_sync();
+            uint32_t v[4][32];
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                ptx::tmem_wait_ld(v[cc]);
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&c.tempty[0]);
+            ++tiles_done;
+            if (r < t.rows) {
+                const int64_t off = (t.row0 + r) * ld + t.col0 + 128 * h;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (OUT_BF16)
+                        store_row_bf16(static_cast<uint16_t*>(p.out) + off + 32 * cc, v[cc]);
+                    else
+                        store_row_f32(static_cast<float*>(p.out) + off + 32 * cc, v[cc]);
+                }
+            }
+        }
+    } else if (warp >= 4 && BN == 128) {
         // ------------------------------------------ fprop/dgrad epilogue --
         const int q = warp & 3;
         const int r = 32 * q + lane;        // row of the tile this thread writes
@@ -663,6 +707,12 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
 #define GQ_PAIRS 0
 #endif
 constexpr bool kUsePairs = GQ_PAIRS != 0;
+// Whether fprop/dgrad use single-CTA 128 x 256 tiles where the output width
+// allows (tuning knob).
+#ifndef GQ_WIDE
+#define GQ_WIDE 1
+#endif
+constexpr bool kWideTiles = GQ_WIDE != 0;
 constexpr int P_BN = 256;          // N of the pair MMA (output columns per tile)
 constexpr int P_STAGE = 16384 + 16384 + 512 + 1024;   // A half, B half, SFA atom, 2 SFB atoms
 constexpr int P_STAGES = 6;
@@ -1146,7 +1196,7 @@ gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap
     if (prepare(kernel, S::SMEM) != cudaSuccess)
         return GQ_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
-    kernel<<<(unsigned)grid, 256, S::SMEM, stream>>>(ma, mb, mo, args);
+    kernel<<<(unsigned)grid, S::THREADS, S::SMEM, stream>>>(ma, mb, mo, args);
     return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 
@@ -1238,6 +1288,17 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                                                   : run_mx2<GEMM_FPROP, false>(ma, mb, msa, msb, args, bound, stream);
             return out_dtype == GQ_DTYPE_BF16 ? run_mx2<GEMM_DGRAD, true>(ma, mb, msa, msb, args, bound, stream)
                                               : run_mx2<GEMM_DGRAD, false>(ma, mb, msa, msb, args, bound, stream);
+        }
+        if (kWideTiles && n_out % 256 == 0) {
+            // 128 x 256 tiles: B of fprop travels as one 256-row box
+            if (kind == GEMM_FPROP && !make_map_u8(&mb, b.data, b.rows, b.cols, 256))
+                return GQ_ERR_CUDA;
+            const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 256);
+            if (kind == GEMM_FPROP)
+                return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_FPROP, 256, true>(ma, mb, ma, args, bound, stream)
+                                                  : run_mx<GEMM_FPROP, 256, false>(ma, mb, ma, args, bound, stream);
+            return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_DGRAD, 256, true>(ma, mb, ma, args, bound, stream)
+                                              : run_mx<GEMM_DGRAD, 256, false>(ma, mb, ma, args, bound, stream);
         }
         const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 128);
         if (kind == GEMM_FPROP)
