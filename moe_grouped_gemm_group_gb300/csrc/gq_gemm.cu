@@ -80,7 +80,7 @@ struct MxShape {
     static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     // wgrad stages its fp32 output tile in shared memory (TMA load of the
     // old main grad, TMA store of the result): BN / 32 boxes of 128 x 32.
-    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? BM * BN * 4 : 0;
+    static constexpr int OUT_BYTES = (KIND == GEMM_WGRAD_MX && BN == 128) ? BM * BN * 4 : 0;
     static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
     // Scale factors rotate through SF_SLOTS column groups, so that the copy
     // for k-tile i + 1 never overwrites columns the MMAs of k-tile i still
@@ -236,6 +236,18 @@ __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t (&r
         }
         d[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+// dst[0..31] += r[0..31] as eight 16-byte reductions performed at L2 (one
+// add per element, so the result is deterministic).
+__device__ __forceinline__ void reduce_row_f32(float* dst, const uint32_t (&r)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i),
+                     "f"(__uint_as_float(r[4 * i])), "f"(__uint_as_float(r[4 * i + 1])),
+                     "f"(__uint_as_float(r[4 * i + 2])), "f"(__uint_as_float(r[4 * i + 3]))
+                     : "memory");
 }
 
 __device__ __forceinline__ void accumulate_row_f32(float* dst, const uint32_t (&r)[32])
@@ -448,7 +460,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         ptx::tc_commit(c.drain);
         volatile int no_abort = 0;
         ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
-    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
+    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX && BN == 128) {
         // ------------------------------------------- wgrad epilogue --
         // The fp32 output tile moves through a ring of four 128-byte-swizzled
         // shared boxes of 128 rows x 32 columns (one per 32-column slice of
@@ -581,18 +593,29 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::bulk_wait_all();
         }
     } else if (warp >= 4 && BN == 256) {
-        // ------------------------------ fprop/dgrad epilogue, 256 columns --
+        // ------------------------------------- epilogue, 256 columns --
         // One accumulator fills TMEM, so it is drained into registers (each
         // of 8 warps takes its lane quadrant's 32 rows x 128 columns) and
         // handed back before the stores; the next tile's MMAs overlap them.
+        // The wgrad adds into the fp32 main grad with vector reductions at
+        // L2 (accumulate) or stores it (accumulate == 0).
         const int q = warp & 3, h = (warp - 4) >> 2;
         const int r = 32 * q + lane;
         const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
         int64_t tiles_done = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
-            if (t.skip || t.nk == 0)
+            if (t.skip)
                 continue;
+            if (t.nk == 0) {                 // wgrad, empty group, accumulate == 0: +0.0
+                float* dst = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k +
+                             t.col0 + 128 * h;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    reinterpret_cast<float4*>(dst)[i] = z;
+                continue;
+            }
             if (!ptx::mbar_wait(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
                 break;
             ptx::tc_fence_after_sync();
@@ -609,7 +632,17 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (lane == 0)
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
-            if (r < t.rows) {
+            if (KIND == GEMM_WGRAD_MX) {
+                float* dst = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k +
+                             t.col0 + 128 * h;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (p.accumulate)
+                        reduce_row_f32(dst + 32 * cc, v[cc]);
+                    else
+                        store_row_f32(dst + 32 * cc, v[cc]);
+                }
+            } else if (r < t.rows) {
                 const int64_t off = (t.row0 + r) * ld + t.col0 + 128 * h;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -1310,6 +1343,10 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
     case GEMM_WGRAD_MX: {
         if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
+        if (kWideTiles && k % 256 == 0) {
+            const int64_t bound = (int64_t)G * (n / 128) * (k / 256);
+            return run_mx<GEMM_WGRAD_MX, 256, false>(ma, mb, ma, args, bound, stream);
+        }
         CUtensorMap mo;
         if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, 128))
             return GQ_ERR_CUDA;
