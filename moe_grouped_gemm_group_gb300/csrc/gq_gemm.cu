@@ -80,7 +80,9 @@ struct MxShape {
     static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     // wgrad stages its fp32 output tile in shared memory (TMA load of the
     // old main grad, TMA store of the result): BN / 32 boxes of 128 x 32.
-    static constexpr int OUT_BYTES = (KIND == GEMM_WGRAD_MX && BN == 128) ? BM * BN * 4 : 0;
+    // (four 128 x 32 fp32 boxes: one ring of four for BN = 128, two rings of
+    // two -- one per half of the tile's columns -- for BN = 256).
+    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? 4 * BM * 128 : 0;
     static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
     // Scale factors rotate through SF_SLOTS column groups, so that the copy
     // for k-tile i + 1 never overwrites columns the MMAs of k-tile i still
@@ -91,7 +93,7 @@ struct MxShape {
     static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales, slot 0
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 5) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1) + 16;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - OUT_BYTES - SCAN_BYTES - BAR_BYTES) / STAGE;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
@@ -112,7 +114,6 @@ struct Carve {
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
-    uint64_t* ofull;      // [4] old output boxes landed (wgrad accumulate)
     uint32_t* tmem_base;
     volatile int* abort;
     int64_t* s_off;
@@ -143,8 +144,7 @@ __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, in
     c.tfull = c.empty + 8;
     c.tempty = c.tfull + acc;
     c.drain = c.tempty + acc;
-    c.ofull = c.drain + 1;
-    c.tmem_base = reinterpret_cast<uint32_t*>(c.ofull + 4);
+    c.tmem_base = reinterpret_cast<uint32_t*>(c.drain + 1);
     c.abort = reinterpret_cast<volatile int*>(c.tmem_base + 1);
     c.s_off = reinterpret_cast<int64_t*>(c.tmem_base + 4);
     c.s_tp = reinterpret_cast<int32_t*>(c.s_off + GQ_MAX_GROUPS + 1);
@@ -238,29 +238,6 @@ __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t (&r
     }
 }
 
-// dst[0..31] += r[0..31] as eight 16-byte reductions performed at L2 (one
-// add per element, so the result is deterministic).
-__device__ __forceinline__ void reduce_row_f32(float* dst, const uint32_t (&r)[32])
-{
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i),
-                     "f"(__uint_as_float(r[4 * i])), "f"(__uint_as_float(r[4 * i + 1])),
-                     "f"(__uint_as_float(r[4 * i + 2])), "f"(__uint_as_float(r[4 * i + 3]))
-                     : "memory");
-}
-
-__device__ __forceinline__ void accumulate_row_f32(float* dst, const uint32_t (&r)[32])
-{
-    float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 o = d[i];
-        d[i] = make_float4(o.x + __uint_as_float(r[4 * i]), o.y + __uint_as_float(r[4 * i + 1]),
-                           o.z + __uint_as_float(r[4 * i + 2]), o.w + __uint_as_float(r[4 * i + 3]));
-    }
-}
-
 // Wait for the TMA writes of the last min(stages, issued) issued stages, so
 // that none lands after the CTA has left (bounded; used on every exit path).
 __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t issued,
@@ -308,8 +285,6 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::mbar_init(&c.tempty[a], S::EPI_WARPS);
         }
         ptx::mbar_init(c.drain, 1);
-        for (int i = 0; i < 4; ++i)
-            ptx::mbar_init(c.ofull + i, 1);
         *c.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -460,162 +435,102 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         ptx::tc_commit(c.drain);
         volatile int no_abort = 0;
         ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
-    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX && BN == 128) {
-        // ------------------------------------------- wgrad epilogue --
-        // The fp32 output tile moves through a ring of four 128-byte-swizzled
-        // shared boxes of 128 rows x 32 columns (one per 32-column slice of
-        // the accumulator).  The lead thread keeps TMA loads of the old main
-        // grad (accumulate) up to three boxes ahead, across tile boundaries;
-        // for each box the 128 epilogue threads add their TMEM row into the
-        // box and the lead TMA-stores it.  A slot is reloaded only after the
-        // store that last read it has finished reading (bulk wait_group.read).
-        const int q = warp & 3;
+    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
+        // ------------------------------------------------ wgrad epilogue --
+        // The tile's fp32 result leaves through 128 x 32 boxes in shared
+        // memory (128-byte swizzle): the epilogue threads copy TMEM columns
+        // into a box and one lead thread hands it to the TMA unit -- a plain
+        // store (accumulate == 0) or a reduction that adds it into the main
+        // grad at L2 (accumulate == 1), one add per element, so repeated
+        // calls are bitwise identical.  No old value passes through the SM.
+        // BN = 128: 4 warps, one ring of four boxes.  BN = 256: 8 warps in
+        // two halves of 128 columns, each with a ring of two boxes; halves
+        // meet on named barriers 1 and 2.
+        constexpr int HALVES = S::EPI_WARPS / 4;
+        constexpr int SLOTS = 4 / HALVES;                 // boxes per ring
+        constexpr int BOX = BM * 128;
+        const int q = warp & 3, h = (warp - 4) >> 2;
         const uint32_t r = 32 * q + lane;
-        const bool lead = (warp == 4 && lane == 0);
-        constexpr int NB = BN / 32;                 // boxes per tile
-        constexpr int BOX = BM * 128;               // bytes per box
-        int64_t tiles_done = 0;
-        int64_t q_proc = 0, q_load = 0;             // boxes processed / loads issued
-        int64_t ld_tile = blockIdx.x;               // tile cursor of the load issuer
-        int ld_box = 0;
-        // Issue old-value loads until `ahead` boxes beyond q_proc are in flight.
-        auto issue_loads = [&](int64_t limit) {
-            while (q_load < limit) {
-                while (ld_tile < ntiles) {          // skip tiles without output
-                    const Tile lt = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, ld_tile);
-                    if (!lt.skip)
-                        break;
-                    ld_tile += gridDim.x;
-                }
-                if (ld_tile >= ntiles)
-                    return;
-                const Tile lt = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, ld_tile);
-                // the slot last held box q_load - 4, whose store has been committed
-                // among the q_proc groups so far: allow the newer ones to pend
-                if (q_load >= 4) {
-                    const int64_t pend = q_proc - (q_load - 4) - 1;
-                    if (pend <= 0)
-                        ptx::bulk_wait_read_all();
-                    else if (pend == 1)
-                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                    else if (pend == 2)
-                        asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
-                    else
-                        asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
-                }
-                const int slot = (int)(q_load & 3);
-                uint64_t* ob = c.ofull + slot;
-                ptx::mbar_arrive_expect_tx(ob, BOX);
-                ptx::tma_load_2d(c.out + slot * BOX, &tma_o, ob, (int32_t)(lt.col0 + 32 * ld_box),
-                                 (int32_t)((int64_t)lt.g * p.n + lt.mt * BM));
-                ++q_load;
-                if (++ld_box == NB) {
-                    ld_box = 0;
-                    ld_tile += gridDim.x;
-                }
-            }
-        };
+        const bool lead = lane == 0 && q == 0;
+        const int bar_id = 1 + h;
+        uint8_t* ring = c.out + h * SLOTS * BOX;
+        int64_t tiles_done = 0, q_proc = 0;
         bool stop = false;
         for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
             if (t.skip)
                 continue;
             const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM);
-            const int acc = (int)(tiles_done % S::ACC);
-            const uint32_t acc_ph = (uint32_t)((tiles_done / S::ACC) & 1);
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
             bool ok = true;
-            if (t.nk > 0)
-                ok = ptx::mbar_wait(&c.tfull[acc], acc_ph, c.abort, p.status);
-            if (ok && t.nk > 0)
-                ptx::tc_fence_after_sync();
+            if (t.nk > 0) {
+                ok = ptx::mbar_wait(&c.tfull[tiles_done % S::ACC], (uint32_t)((tiles_done / S::ACC) & 1),
+                                    c.abort, p.status);
+                if (ok)
+                    ptx::tc_fence_after_sync();
+            }
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) +
+                                (uint32_t)(tiles_done % S::ACC) * BN + 128 * h;
 #pragma unroll 1
-            for (int cc = 0; cc < NB; ++cc, ++q_proc) {
-                const int slot = (int)(q_proc & 3);
-                if (p.accumulate) {
-                    if (lead)
-                        issue_loads(q_proc + 4);
-                    if (ok)
-                        ok = ptx::mbar_wait(c.ofull + slot, (uint32_t)((q_proc >> 2) & 1), c.abort,
-                                            p.status);
-                } else if (lead) {
-                    // the store of box q_proc - 4 read this slot; newer ones may pend
-                    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+            for (int cc = 0; cc < 4; ++cc, ++q_proc) {        // each half: 128 columns
+                const int slot = (int)(q_proc % SLOTS);
+                if (lead) {
+                    // the store of box q_proc - SLOTS read this slot; newer ones may pend
+                    if (SLOTS == 4)
+                        asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+                    else
+                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                 }
-                if (ptx::named_barrier_or(1, 128, !ok)) {
+                if (ptx::named_barrier_or(bar_id, 128, !ok)) {
                     stop = true;
                     break;
                 }
                 uint32_t v[32];
                 if (t.nk > 0) {
-                    ptx::tmem_ld_32x32(tbase + 32 * cc, v);
+                    ptx::tmem_ld_32x32(tb + 32 * cc, v);
                     ptx::tmem_wait_ld(v);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = 0u;
                 }
-                const uint32_t box = ptx::smem_addr(c.out + slot * BOX);
+                const uint32_t box = ptx::smem_addr(ring + slot * BOX);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t addr = box + ptx::swz128(r, j);
-                    uint4 o = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    if (p.accumulate) {
-                        const uint4 old = ptx::lds128(addr);
-                        o.x = __float_as_uint(__uint_as_float(old.x) + __uint_as_float(o.x));
-                        o.y = __float_as_uint(__uint_as_float(old.y) + __uint_as_float(o.y));
-                        o.z = __float_as_uint(__uint_as_float(old.z) + __uint_as_float(o.z));
-                        o.w = __float_as_uint(__uint_as_float(old.w) + __uint_as_float(o.w));
-                    }
-                    ptx::sts128(addr, o);
-                }
-                if (cc == NB - 1 && t.nk > 0) {
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(&c.tempty[acc]);
-                }
+                for (int j = 0; j < 8; ++j)
+                    ptx::sts128(box + ptx::swz128(r, j), make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                 ptx::fence_proxy_async_smem();
-                ptx::named_barrier_or(1, 128, 0);
+                ptx::named_barrier_or(bar_id, 128, 0);
                 if (lead) {
-                    ptx::tma_store_2d(&tma_o, c.out + slot * BOX, (int32_t)(t.col0 + 32 * cc), orow);
+                    const int32_t col = (int32_t)(t.col0 + 128 * h + 32 * cc);
+                    if (p.accumulate)
+                        ptx::tma_reduce_add_2d(&tma_o, ring + slot * BOX, col, orow);
+                    else
+                        ptx::tma_store_2d(&tma_o, ring + slot * BOX, col, orow);
                     ptx::bulk_commit_group();
                 }
             }
-            if (t.nk > 0)
+            if (t.nk > 0 && !stop) {
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(&c.tempty[tiles_done % S::ACC]);
                 ++tiles_done;
+            }
         }
-        if (lead) {
-            volatile int no_abort = 0;
-            for (int64_t qq = q_proc; qq < q_load; ++qq)      // loads issued but not consumed
-                if (!ptx::mbar_wait(c.ofull + (qq & 3), (uint32_t)((qq >> 2) & 1), &no_abort, p.status))
-                    break;
+        if (lead)
             ptx::bulk_wait_all();
-        }
-    } else if (warp >= 4 && BN == 256) {
-        // ------------------------------------- epilogue, 256 columns --
+    } else if (warp >= 4 && BN == 256 && KIND != GEMM_WGRAD_MX) {
+        // ------------------------------ fprop/dgrad epilogue, 256 columns --
         // One accumulator fills TMEM, so it is drained into registers (each
         // of 8 warps takes its lane quadrant's 32 rows x 128 columns) and
         // handed back before the stores; the next tile's MMAs overlap them.
-        // The wgrad adds into the fp32 main grad with vector reductions at
-        // L2 (accumulate) or stores it (accumulate == 0).
         const int q = warp & 3, h = (warp - 4) >> 2;
         const int r = 32 * q + lane;
         const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
         int64_t tiles_done = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
-            if (t.skip)
+            if (t.skip || t.nk == 0)
                 continue;
-            if (t.nk == 0) {                 // wgrad, empty group, accumulate == 0: +0.0
-                float* dst = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k +
-                             t.col0 + 128 * h;
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    reinterpret_cast<float4*>(dst)[i] = z;
-                continue;
-            }
             if (!ptx::mbar_wait(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
                 break;
             ptx::tc_fence_after_sync();
@@ -632,17 +547,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (lane == 0)
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
-            if (KIND == GEMM_WGRAD_MX) {
-                float* dst = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k +
-                             t.col0 + 128 * h;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    if (p.accumulate)
-                        reduce_row_f32(dst + 32 * cc, v[cc]);
-                    else
-                        store_row_f32(dst + 32 * cc, v[cc]);
-                }
-            } else if (r < t.rows) {
+            if (r < t.rows) {
                 const int64_t off = (t.row0 + r) * ld + t.col0 + 128 * h;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -653,7 +558,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 }
             }
         }
-    } else if (warp >= 4 && BN == 128) {
+    } else if (warp >= 4 && BN == 128 && KIND != GEMM_WGRAD_MX) {
         // ------------------------------------------ fprop/dgrad epilogue --
         const int q = warp & 3;
         const int r = 32 * q + lane;        // row of the tile this thread writes
@@ -664,21 +569,11 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 continue;
             float* out32 = nullptr;
             uint16_t* out16 = nullptr;
-            if (KIND == GEMM_FPROP || KIND == GEMM_DGRAD) {
-                const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
-                if (OUT_BF16)
-                    out16 = static_cast<uint16_t*>(p.out) + (t.row0 + r) * ld + t.col0;
-                else
-                    out32 = static_cast<float*>(p.out) + (t.row0 + r) * ld + t.col0;
-            } else {
-                out32 = static_cast<float*>(p.out) + ((int64_t)t.g * p.n + t.mt * BM + r) * p.k + t.col0;
-            }
-            if (t.nk == 0) {                 // empty group, accumulate == 0: write +0.0
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int i = 0; i < BN / 4; ++i)
-                    reinterpret_cast<float4*>(out32)[i] = z;
-                continue;
-            }
+            const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
+            if (OUT_BF16)
+                out16 = static_cast<uint16_t*>(p.out) + (t.row0 + r) * ld + t.col0;
+            else
+                out32 = static_cast<float*>(p.out) + (t.row0 + r) * ld + t.col0;
             const int acc = (int)(tiles_done % S::ACC);
             const uint32_t acc_ph = (uint32_t)((tiles_done / S::ACC) & 1);
             if (!ptx::mbar_wait(&c.tfull[acc], acc_ph, c.abort, p.status))
@@ -694,8 +589,6 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 if (live) {
                     if (OUT_BF16)
                         store_row_bf16(out16 + 32 * cc, v);
-                    else if (KIND == GEMM_WGRAD_MX && p.accumulate)
-                        accumulate_row_f32(out32 + 32 * cc, v);
                     else
                         store_row_f32(out32 + 32 * cc, v);
                 }
@@ -1016,7 +909,7 @@ struct ChShape {
     static constexpr int PBUF = 2;
     static constexpr uint32_t TMEM_COLS = 256;
     static constexpr int SCAN_BYTES = MxShape<GEMM_FPROP, 128>::SCAN_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * PBUF + 5) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * PBUF + 1) + 16;
     static constexpr int STAGES = 6;
     static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + SCAN_BYTES;
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
@@ -1343,13 +1236,13 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
     case GEMM_WGRAD_MX: {
         if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
-        if (kWideTiles && k % 256 == 0) {
-            const int64_t bound = (int64_t)G * (n / 128) * (k / 256);
-            return run_mx<GEMM_WGRAD_MX, 256, false>(ma, mb, ma, args, bound, stream);
-        }
         CUtensorMap mo;
         if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, 128))
             return GQ_ERR_CUDA;
+        if (kWideTiles && k % 256 == 0) {
+            const int64_t bound = (int64_t)G * (n / 128) * (k / 256);
+            return run_mx<GEMM_WGRAD_MX, 256, false>(ma, mb, mo, args, bound, stream);
+        }
         const int64_t bound = (int64_t)G * (n / 128) * (k / 128);
         return run_mx<GEMM_WGRAD_MX, 128, false>(ma, mb, mo, args, bound, stream);
     }
