@@ -153,6 +153,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
         : "memory");
 }
 
+// Contiguous shared -> global copy (both 16-byte aligned, size % 16 == 0),
+// as part of the current bulk-async group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -112,7 +112,10 @@ __global__ void k_split_scan(const int32_t* __restrict__ splits, int G, int64_t 
 
 // Shared-memory plan of k_quant_mx: a ring of kQStages input tiles, each a
 // 128-row x 128-column bf16 tile loaded by TMA as two 128-byte-swizzled boxes
-// of [128 rows][64 columns]; barriers; the split scan.
+// of [128 rows][64 columns]; two output staging buffers, each holding the
+// tile's rowwise and columnwise codes (128-byte-swizzled [128 rows][128 B])
+// and its two 512-byte scale atoms; the column-scale broadcast area;
+// barriers; the split scan.
 // Ring depth and CTAs per SM (tuning knobs; the defaults are the measured best).
 #ifndef GQ_Q_STAGES
 #define GQ_Q_STAGES 4
@@ -122,23 +125,34 @@ __global__ void k_split_scan(const int32_t* __restrict__ splits, int G, int64_t 
 #endif
 constexpr int kQStages = GQ_Q_STAGES;
 constexpr int kQTile = 128 * 128 * 2;
+constexpr int kQOut = 128 * 128;                       // one orientation's codes
+constexpr int kQStageOut = 2 * kQOut + 1024;           // row codes, col codes, 2 atoms
 constexpr int kQConsumers = 512;                       // 16 consumer warps
 constexpr int kQThreadsMx = kQConsumers + 32;          // + 1 producer warp
 constexpr int kQScanBytes = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
-constexpr int kQSmem = 1024 + kQStages * kQTile + 16 * 32 * 4 + 8 * 2 * kQStages + 16 + kQScanBytes;
+constexpr int kQSmem = 1024 + kQStages * kQTile + 2 * kQStageOut + 16 * 32 * 4 + 8 * 2 * kQStages + 16 +
+                       kQScanBytes;
+
+// Output tensor maps of k_quant_mx: codes of one orientation as [rows, cols]
+// uint8 with 128-byte swizzle, boxes of 128 columns x 128 rows (whole tiles)
+// and 128 columns x 32 rows (the live part of a group's last tile).
+struct QuantOutMaps {
+    CUtensorMap row128, row32, col128, col32;
+};
 
 template <bool ROW, bool COL>
 __global__ void __launch_bounds__(kQThreadsMx, GQ_Q_MINB)
-k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t cols,
-           const int32_t* __restrict__ splits, int G, uint8_t* __restrict__ row_data,
-           uint8_t* __restrict__ row_scale, uint8_t* __restrict__ col_data,
-           uint8_t* __restrict__ col_scale, int32_t* __restrict__ status)
+k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ QuantOutMaps om,
+           int64_t rows_cap, int64_t cols, const int32_t* __restrict__ splits, int G,
+           uint8_t* __restrict__ row_scale, uint8_t* __restrict__ col_scale,
+           int32_t* __restrict__ status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* tiles = base;
-    float* s_inv = reinterpret_cast<float*>(tiles + kQStages * kQTile);  // [16 warps][32] column 2^-e
+    uint8_t* outs = tiles + kQStages * kQTile;                       // [2][kQStageOut]
+    float* s_inv = reinterpret_cast<float*>(outs + 2 * kQStageOut);  // [16 warps][32] column 2^-e
     uint64_t* full = reinterpret_cast<uint64_t*>(s_inv + 16 * 32);
     uint64_t* empty = full + kQStages;
     volatile int* abort = reinterpret_cast<volatile int*>(empty + kQStages);
@@ -197,8 +211,15 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t 
     }
 
     // ---------------------------------------------------------- consumers --
+    // Each tile's codes and scale atoms are staged in shared memory (double
+    // buffered) and leave as whole 128-byte lines: TMA stores for the codes,
+    // bulk copies for the atoms, all issued by consumer thread 0 after the
+    // consumers' barrier.  Before that barrier thread 0 waits until the
+    // previous tile's stores have read their buffer, which frees the buffer
+    // the next tile writes.
     const int rb = warp >> 2, cb = warp & 3;
     const uint32_t r_in_tile = 32 * rb + lane;
+    const bool lead = threadIdx.x == 0;
     int64_t it = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
         const int s = (int)(it % kQStages);
@@ -208,10 +229,11 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t 
         const int g = group_of_tile(s_tp, G, rt);
         const int64_t lt = rt - s_tp[g];
         const int64_t m = s_off[g + 1] - s_off[g];
-        const int64_t rows_here = min((int64_t)128, m - 128 * lt);   // a multiple of 32
+        const int rows_here = (int)min((int64_t)128, m - 128 * lt);   // a multiple of 32
         const bool active = 32 * rb < rows_here;                     // uniform per warp
-        const int64_t row = s_off[g] + 128 * lt + r_in_tile;
-        const int64_t col0 = (int64_t)ct * 128 + 32 * cb;
+        uint8_t* ob = outs + (it & 1) * kQStageOut;
+        const uint32_t rd_box = ptx::smem_addr(ob), cd_box = ptx::smem_addr(ob + kQOut);
+        uint8_t* atoms = ob + 2 * kQOut;                                 // [row 512 | col 512]
 
         const bool ok = ptx::mbar_wait(&full[s], ph, abort, status);
         uint32_t v[16];
@@ -255,7 +277,9 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t 
                 for (int i = 0; i < 8; ++i)
                     w[i] = cvt_e4m3x2(xf[4 * i] * sc, xf[4 * i + 1] * sc) |
                            (cvt_e4m3x2(xf[4 * i + 2] * sc, xf[4 * i + 3] * sc) << 16);
-                store32(row_data + row * cols + col0, w);
+                // 32 codes = 16-byte chunks 2 cb and 2 cb + 1 of the row
+                ptx::sts128(rd_box + ptx::swz128(r_in_tile, 2 * cb), make_uint4(w[0], w[1], w[2], w[3]));
+                ptx::sts128(rd_box + ptx::swz128(r_in_tile, 2 * cb + 1), make_uint4(w[4], w[5], w[6], w[7]));
             }
             if (COL) {
                 // Transpose-max across the warp: after exchanging half of the
@@ -307,23 +331,46 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, int64_t rows_cap, int64_t 
                 for (int i = 0; i < 8; ++i)
                     w[i] = cvt_e4m3x2(xf[4 * i] * sc[4 * i], xf[4 * i + 1] * sc[4 * i + 1]) |
                            (cvt_e4m3x2(xf[4 * i + 2] * sc[4 * i + 2], xf[4 * i + 3] * sc[4 * i + 3]) << 16);
-                store32(col_data + row * cols + col0, w);
+                ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb), make_uint4(w[0], w[1], w[2], w[3]));
+                ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb + 1), make_uint4(w[4], w[5], w[6], w[7]));
             }
         }
-        if (!ok)
+        // Scale atoms: rowwise (row 32 rb + lane, block cb), columnwise
+        // (channel 32 cb + lane, 32-row block rb); inactive warps write the
+        // zero entries of a partial last tile.  16 warps cover each atom once.
+        atoms[lane * 16 + rb * 4 + cb] = (uint8_t)rbyte;
+        atoms[512 + lane * 16 + cb * 4 + rb] = (uint8_t)cbyte;
+        ptx::fence_proxy_async_smem();
+        if (lead)
+            ptx::bulk_wait_read_all();      // the previous tile's stores have read their buffer
+        if (ptx::named_barrier_or(1, kQConsumers, !ok))
             break;
-        // Scale bytes go straight to their atoms: rowwise (row 32 rb + lane,
-        // block cb), columnwise (channel 32 cb + lane, 32-row block rb).
-        // Inactive warps write the zero entries of a partial last tile.  The
-        // 16 warps together cover each 512-byte atom once.
-        const int64_t sbase = 512 * (int64_t)nct * s_tp[g];
-        if (ROW)
-            row_scale[sbase + (lt * nct + ct) * 512 + lane * 16 + rb * 4 + cb] = (uint8_t)rbyte;
-        if (COL) {
-            const int64_t T = s_tp[g + 1] - s_tp[g];
-            col_scale[sbase + ((int64_t)ct * T + lt) * 512 + lane * 16 + cb * 4 + rb] = (uint8_t)cbyte;
+        if (lead) {
+            const int32_t row0 = (int32_t)(s_off[g] + 128 * lt);
+            const int32_t x = ct * 128;
+            const int64_t sbase = 512 * (int64_t)nct * s_tp[g];
+            if (ROW) {
+                if (rows_here == 128)
+                    ptx::tma_store_2d(&om.row128, ob, x, row0);
+                else
+                    for (int k = 0; k < rows_here / 32; ++k)
+                        ptx::tma_store_2d(&om.row32, ob + k * 32 * 128, x, row0 + 32 * k);
+                ptx::bulk_store(row_scale + sbase + (lt * nct + ct) * 512, atoms, 512);
+            }
+            if (COL) {
+                if (rows_here == 128)
+                    ptx::tma_store_2d(&om.col128, ob + kQOut, x, row0);
+                else
+                    for (int k = 0; k < rows_here / 32; ++k)
+                        ptx::tma_store_2d(&om.col32, ob + kQOut + k * 32 * 128, x, row0 + 32 * k);
+                const int64_t T = s_tp[g + 1] - s_tp[g];
+                ptx::bulk_store(col_scale + sbase + ((int64_t)ct * T + lt) * 512, atoms + 512, 512);
+            }
+            ptx::bulk_commit_group();
         }
     }
+    if (lead)
+        ptx::bulk_wait_all();
 }
 
 __global__ void __launch_bounds__(kQuantThreads, 2)
@@ -419,7 +466,14 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const
                             uint8_t* col_scale, int32_t* status, cudaStream_t stream)
 {
     CUtensorMap map;
+    QuantOutMaps om;
     if (!make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows_cap, cols, 64, 128))
+        return cudaErrorInvalidValue;
+    // unused orientations get a valid (never used) map
+    const uint8_t* rd = row_data ? row_data : col_data;
+    const uint8_t* cd = col_data ? col_data : row_data;
+    if (!make_map_u8(&om.row128, rd, rows_cap, cols, 128) || !make_map_u8(&om.row32, rd, rows_cap, cols, 32) ||
+        !make_map_u8(&om.col128, cd, rows_cap, cols, 128) || !make_map_u8(&om.col32, cd, rows_cap, cols, 32))
         return cudaErrorInvalidValue;
     const int64_t tiles_bound = ((rows_cap + 127) / 128 + G) * (cols / 128);
     const int sms = device_info().sm_count;
@@ -432,8 +486,8 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const
             per_sm < 1)
             per_sm = 1;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, tiles_bound));
-        kernel<<<(unsigned)grid, kQThreadsMx, kQSmem, stream>>>(map, rows_cap, cols, splits, G, row_data,
-                                                                row_scale, col_data, col_scale, status);
+        kernel<<<(unsigned)grid, kQThreadsMx, kQSmem, stream>>>(map, om, rows_cap, cols, splits, G, row_scale,
+                                                                col_scale, status);
         return cudaGetLastError();
     };
     if (row_data && col_data)
