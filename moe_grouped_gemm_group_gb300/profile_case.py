@@ -13,6 +13,8 @@ larger than the 129 MB L2):
               ([66560, 7168] bf16, 65536 live rows)
   fprop       moe_e64_zipf fc1 fprop (n 2048, k 7168, bf16 output)
   dgrad       moe_e64_zipf fc1 dgrad (bf16 output)
+  fprop2      moe_e64_zipf fc2 fprop (n 7168, k 2048, bf16 output)
+  dgrad2      moe_e64_zipf fc2 dgrad (bf16 output)
   wgrad       moe_e8 fc1 k-grouped wgrad accumulating into fp32 (8 x 2048 x 4096)
   wgrad_ch    kgrouped_zero_channel per-channel wgrad (4 x 2048 x 2048)
 Prints the mean CUDA-event time per launch.
@@ -30,7 +32,7 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["quant", "fprop", "dgrad", "wgrad", "wgrad_ch"])
+    ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad_ch"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
 
@@ -58,18 +60,20 @@ def main():
         x = W.device_activation(w, H, 0, device=dev)
         q = gq.alloc_quantized(R, H, E, mx, dev)
         fn = lambda: gq.gq_quantize(x, sp, E, mx, q, st)  # noqa: E731
-    elif args.case in ("fprop", "dgrad"):
-        wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
+    elif args.case in ("fprop", "dgrad", "fprop2", "dgrad2"):
+        # fc1: Y = X W1^T with n = ffn, k = hidden; fc2: n = hidden, k = ffn
+        n, k = (F, H) if args.case in ("fprop", "dgrad") else (H, F)
+        wt = W.device_normal_bf16((E * n, k), w.seed, 0.02, 10, dev)
         qw = quant(wt, None)
         del wt
-        if args.case == "fprop":
-            qx = quant(W.device_activation(w, H, 0, device=dev), sp)
-            y = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
-            fn = lambda: gq.gq_gemm_fprop(qx, qw, sp, E, F, H, y, gq.DTYPE_BF16, st)  # noqa: E731
+        if args.case.startswith("fprop"):
+            qx = quant(W.device_activation(w, k, 0, device=dev), sp)
+            y = torch.empty((R, n), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_fprop(qx, qw, sp, E, n, k, y, gq.DTYPE_BF16, st)  # noqa: E731
         else:
-            qd = quant(W.device_activation(w, F, 2, device=dev), sp)
-            dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
-            fn = lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, F, H, dx, gq.DTYPE_BF16, st)  # noqa: E731
+            qd = quant(W.device_activation(w, n, 2, device=dev), sp)
+            dx = torch.empty((R, k), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, n, k, dx, gq.DTYPE_BF16, st)  # noqa: E731
     elif args.case == "wgrad":
         qx = quant(W.device_activation(w, H, 0, device=dev), sp)
         qd = quant(W.device_activation(w, F, 2, device=dev), sp)
