@@ -29,10 +29,14 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code)
 // a multiple of `align`, or the splits sum past rows_cap; every thread gets
 // the same value.  blockDim.x must be a multiple of 32.
 //
+// OffT is int64_t, or int32_t where the caller has bounded rows_cap below
+// 2^31 (offsets never pass rows_cap: a larger sum is a split error).
+//
 // With `s_tq` non-null it also receives the prefix sums of the 256-row tile
 // counts ceil(m_g / 256) (tiles of a CTA pair); s_w32 then needs 64 entries.
+template <typename OffT>
 __device__ __forceinline__ int block_scan_splits(const int32_t* __restrict__ splits, int G,
-                                                 int64_t rows_cap, int align, int64_t* s_off,
+                                                 int64_t rows_cap, int align, OffT* s_off,
                                                  int32_t* s_tp, int64_t* s_w64, int32_t* s_w32,
                                                  int32_t* s_tq = nullptr)
 {
@@ -96,7 +100,7 @@ __device__ __forceinline__ int block_scan_splits(const int32_t* __restrict__ spl
         }
         __syncthreads();
         if (g < G) {
-            s_off[g] = carry_rows + (warp > 0 ? s_w64[warp - 1] : 0) + xr - m;
+            s_off[g] = (OffT)(carry_rows + (warp > 0 ? s_w64[warp - 1] : 0) + xr - m);
             s_tp[g] = carry_tiles + (warp > 0 ? s_w32[warp - 1] : 0) + xt - t;
             if (s_tq)
                 s_tq[g] = carry_pairs + (warp > 0 ? s_w32[32 + warp - 1] : 0) + xu - u;
@@ -108,7 +112,7 @@ __device__ __forceinline__ int block_scan_splits(const int32_t* __restrict__ spl
         __syncthreads();
     }
     if (tid == 0) {
-        s_off[G] = carry_rows;
+        s_off[G] = (OffT)carry_rows;
         s_tp[G] = carry_tiles;
         if (s_tq)
             s_tq[G] = carry_pairs;

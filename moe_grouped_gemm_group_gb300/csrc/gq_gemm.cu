@@ -54,6 +54,7 @@ constexpr int BM = 128;     // MMA M (rows of the A side)
 constexpr int PF_DIST = GQ_PF_DIST;
 constexpr int BK = 128;     // k-tile depth in elements (= bytes for e4m3)
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kEpiBox = 32 * 64;   // fprop/dgrad output box per epilogue warp (BN = 256)
 
 struct GemmArgs {
     const int32_t* splits;
@@ -82,7 +83,10 @@ struct MxShape {
     // old main grad, TMA store of the result): BN / 32 boxes of 128 x 32.
     // (four 128 x 32 fp32 boxes: one ring of four for BN = 128, two rings of
     // two -- one per half of the tile's columns -- for BN = 256).
-    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? 4 * BM * 128 : 0;
+    // fprop/dgrad with BN = 256 stage their output too: each of the 8
+    // epilogue warps owns a 2 KB box of 32 rows x 64 bytes (64-byte swizzle).
+    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? 4 * BM * 128
+                                     : (BN == 256 ? kEpiBox * 8 : 0);
     static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
     // Scale factors rotate through SF_SLOTS column groups, so that the copy
     // for k-tile i + 1 never overwrites columns the MMAs of k-tile i still
@@ -92,7 +96,7 @@ struct MxShape {
     static constexpr uint32_t SFA_COL = ACC * BN;                     // TMEM column of A scales, slot 0
     static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales, slot 0
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
+    static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 4 + (GQ_MAX_GROUPS + 2) * 4 + 8 + 32 * 8 + 32 * 4;
     static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1) + 16;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - OUT_BYTES - SCAN_BYTES - BAR_BYTES) / STAGE;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -116,7 +120,7 @@ struct Carve {
     uint64_t* drain;
     uint32_t* tmem_base;
     volatile int* abort;
-    int64_t* s_off;
+    int32_t* s_off;       // group row offsets (rows_cap < 2^31 on every GEMM call)
     int32_t* s_tp;
     int64_t* s_w64;
     int32_t* s_w32;
@@ -146,9 +150,10 @@ __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, in
     c.drain = c.tempty + acc;
     c.tmem_base = reinterpret_cast<uint32_t*>(c.drain + 1);
     c.abort = reinterpret_cast<volatile int*>(c.tmem_base + 1);
-    c.s_off = reinterpret_cast<int64_t*>(c.tmem_base + 4);
-    c.s_tp = reinterpret_cast<int32_t*>(c.s_off + GQ_MAX_GROUPS + 1);
-    c.s_w64 = reinterpret_cast<int64_t*>(c.s_tp + GQ_MAX_GROUPS + 2);
+    c.s_off = reinterpret_cast<int32_t*>(c.tmem_base + 4);
+    c.s_tp = c.s_off + GQ_MAX_GROUPS + 1;
+    c.s_w64 = reinterpret_cast<int64_t*>((reinterpret_cast<uintptr_t>(c.s_tp + GQ_MAX_GROUPS + 2) + 7) &
+                                         ~uintptr_t(7));
     c.s_w32 = reinterpret_cast<int32_t*>(c.s_w64 + 32);
     return c;
 }
@@ -177,7 +182,7 @@ __device__ __forceinline__ int64_t tile_count(const GemmArgs& p, const int32_t* 
 }
 
 template <int KIND, int BN>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& p, const int64_t* s_off,
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& p, const int32_t* s_off,
                                             const int32_t* s_tp, int64_t tile)
 {
     Tile t;
@@ -295,7 +300,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tma_a);
         ptx::prefetch_tmap(&tma_b);
-        if (KIND == GEMM_WGRAD_MX)
+        if (KIND == GEMM_WGRAD_MX || BN == 256)
             ptx::prefetch_tmap(&tma_o);
     }
     ptx::tc_fence_before_sync();
@@ -522,10 +527,20 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // ------------------------------ fprop/dgrad epilogue, 256 columns --
         // One accumulator fills TMEM, so it is drained into registers (each
         // of 8 warps takes its lane quadrant's 32 rows x 128 columns) and
-        // handed back before the stores; the next tile's MMAs overlap them.
+        // handed back at once; the next tile's MMAs overlap the stores.  Each
+        // warp then writes its rows through its own 2 KB box in shared memory
+        // (32 rows x 64 bytes, 64-byte swizzle) that lane 0 hands to the TMA
+        // unit, box after box: whole 64-byte row segments reach L2 instead of
+        // 16-byte pieces of 32 rows per store instruction.  The 32 rows of a
+        // warp are all live or all past the group's end (group sizes are
+        // multiples of 32), so a box is never partial.
+        constexpr int CW = OUT_BF16 ? 32 : 16;           // output columns per box
+        constexpr int NBOX = 128 / CW;
         const int q = warp & 3, h = (warp - 4) >> 2;
-        const int r = 32 * q + lane;
-        const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
+        uint8_t* box = c.out + (warp - 4) * kEpiBox;
+        const uint32_t box_addr = ptx::smem_addr(box);
+        const uint32_t row_addr = box_addr + 64 * lane;  // this lane's row of the box
+        const uint32_t sw = (lane >> 1) & 3;             // 64-byte swizzle of that row
         int64_t tiles_done = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
@@ -547,17 +562,44 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (lane == 0)
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
-            if (r < t.rows) {
-                const int64_t off = (t.row0 + r) * ld + t.col0 + 128 * h;
+            if (32 * q >= t.rows)
+                continue;
+            const int32_t orow = (int32_t)(t.row0 + 32 * q);
+            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    if (OUT_BF16)
-                        store_row_bf16(static_cast<uint16_t*>(p.out) + off + 32 * cc, v[cc]);
-                    else
-                        store_row_f32(static_cast<float*>(p.out) + off + 32 * cc, v[cc]);
+            for (int b = 0; b < NBOX; ++b) {
+                if (lane == 0)
+                    ptx::bulk_wait_read_all();           // the last box's store has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 val;
+                    if (OUT_BF16) {
+                        const uint32_t* src = &v[b][8 * j];
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(src[2 * i]),
+                                                                            __uint_as_float(src[2 * i + 1]));
+                            w[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                        }
+                        val = make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+                        const uint32_t* src = &v[b >> 1][16 * (b & 1) + 4 * j];
+                        val = make_uint4(src[0], src[1], src[2], src[3]);
+                    }
+                    ptx::sts128(row_addr + ((j ^ sw) << 4), val);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&tma_o, box, ocol + CW * b, orow);
+                    ptx::bulk_commit_group();
                 }
             }
         }
+        if (lane == 0)
+            ptx::bulk_wait_all();
     } else if (warp >= 4 && BN == 128 && KIND != GEMM_WGRAD_MX) {
         // ------------------------------------------ fprop/dgrad epilogue --
         const int q = warp & 3;
@@ -1219,12 +1261,18 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
             // 128 x 256 tiles: B of fprop travels as one 256-row box
             if (kind == GEMM_FPROP && !make_map_u8(&mb, b.data, b.rows, b.cols, 256))
                 return GQ_ERR_CUDA;
+            // the output leaves in 32-row boxes of 64 bytes per row
+            const bool bf16 = out_dtype == GQ_DTYPE_BF16;
+            CUtensorMap mo;
+            if (!make_tensor_map_2d_sw64(&mo, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                         bf16 ? 2 : 4, out, rows_cap, n_out, bf16 ? 32 : 16, 32))
+                return GQ_ERR_CUDA;
             const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 256);
             if (kind == GEMM_FPROP)
-                return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_FPROP, 256, true>(ma, mb, ma, args, bound, stream)
-                                                  : run_mx<GEMM_FPROP, 256, false>(ma, mb, ma, args, bound, stream);
-            return out_dtype == GQ_DTYPE_BF16 ? run_mx<GEMM_DGRAD, 256, true>(ma, mb, ma, args, bound, stream)
-                                              : run_mx<GEMM_DGRAD, 256, false>(ma, mb, ma, args, bound, stream);
+                return bf16 ? run_mx<GEMM_FPROP, 256, true>(ma, mb, mo, args, bound, stream)
+                            : run_mx<GEMM_FPROP, 256, false>(ma, mb, mo, args, bound, stream);
+            return bf16 ? run_mx<GEMM_DGRAD, 256, true>(ma, mb, mo, args, bound, stream)
+                        : run_mx<GEMM_DGRAD, 256, false>(ma, mb, mo, args, bound, stream);
         }
         const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 128);
         if (kind == GEMM_FPROP)

@@ -78,6 +78,14 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_by
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool make_tensor_map_2d_sw64(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                             const void* base, int64_t rows, int64_t cols, int box_cols,
+                             int box_rows)
+{
+    return encode_2d(map, dtype, elem_bytes, base, rows, cols, box_cols, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 bool make_tensor_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                               const void* base, int64_t rows, int64_t cols, int box_cols,
                               int box_rows)

@@ -27,6 +27,12 @@ const DeviceInfo& device_info();
 bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                         const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows);
 
+// The same with the 64-byte swizzle (box rows of at most 64 bytes; 16-byte
+// chunk c of box row r sits at chunk c ^ ((r >> 1) & 3) of that row).
+bool make_tensor_map_2d_sw64(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
+                             const void* base, int64_t rows, int64_t cols, int box_cols,
+                             int box_rows);
+
 // The same without swizzle (boxes land row after row in shared memory).
 bool make_tensor_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                               const void* base, int64_t rows, int64_t cols, int box_cols,

@@ -156,18 +156,21 @@ def test_wgrad_matches_oracle(splits, pad, N, K):
     assert_groups_close(got, want, "wgrad")
 
 
-@pytest.mark.parametrize("kind", ["fprop", "dgrad"])
-def test_bf16_output_within_one_ulp(kind):
+@pytest.mark.parametrize("kind,K", [("fprop", 384), ("dgrad", 384), ("fprop", 512), ("dgrad", 512)])
+def test_bf16_output_within_one_ulp(kind, K):
+    """bf16 output: 128- and 256-column tiles (dgrad's output width is K)."""
     splits = np.array([160, 96], np.int32)
-    G, N, K = 2, 256, 384
+    G, N = 2, 256
     a = W.normal_bf16((288, K if kind == "fprop" else N), 11)
     w = W.normal_bf16((G * N, K), 12, scale=0.05)
     if kind == "fprop":
-        got = gpu_fprop(a, w, splits, G, N, K, gq.DTYPE_BF16)[:256]
+        full = gpu_fprop(a, w, splits, G, N, K, gq.DTYPE_BF16)
         want = ora_fprop(a, w, splits, G, N, K)[:256]
     else:
-        got = gpu_dgrad(a, w, splits, G, N, K, gq.DTYPE_BF16)[:256]
+        full = gpu_dgrad(a, w, splits, G, N, K, gq.DTYPE_BF16)
         want = ora_dgrad(a, w, splits, G, N, K)[:256]
+    assert np.all(np.isnan(full[256:])), "wrote rows past the live total"
+    got = full[:256]
     want_b = W.bf16_bits_to_f32(W.f32_to_bf16_bits(want.astype(np.float32))).astype(np.float64)
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - 7)
     assert np.all(np.abs(got - want_b) <= ulp + 1e-30)
