@@ -79,10 +79,9 @@ struct MxShape {
     static constexpr int SFA_BYTES = 512;
     static constexpr int SFB_BYTES = 512 * (BN / 128);
     static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    // wgrad stages its fp32 output tile in shared memory (TMA load of the
-    // old main grad, TMA store of the result): BN / 32 boxes of 128 x 32.
-    // (four 128 x 32 fp32 boxes: one ring of four for BN = 128, two rings of
-    // two -- one per half of the tile's columns -- for BN = 256).
+    // wgrad sends its fp32 output through 64 KB of shared memory on the way
+    // to a TMA store or reduce-add: a ring of four 128 x 32 boxes for
+    // BN = 128, a ring of two 32 x 32 boxes per epilogue warp for BN = 256.
     // fprop/dgrad with BN = 256 stage their output too: each of the 8
     // epilogue warps owns a 2 KB box of 32 rows x 64 bytes (64-byte swizzle).
     static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? 4 * BM * 128
@@ -440,6 +439,76 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         ptx::tc_commit(c.drain);
         volatile int no_abort = 0;
         ptx::mbar_wait(c.drain, 0, &no_abort, p.status);
+    } else if (warp >= 4 && KIND == GEMM_WGRAD_MX && BN == 256) {
+        // ------------------------------------- wgrad epilogue, 256 columns --
+        // One accumulator fills TMEM, so the tile is drained into registers
+        // at once (each of 8 warps takes its lane quadrant's 32 rows x 128
+        // columns) and TMEM goes back to the MMA issuer before any byte moves
+        // to the main grad: the next tile's MMAs overlap this tile's memory
+        // traffic, which is what bounds the k-grouped wgrad.  Each warp then
+        // sends its rows through a ring of two 4 KB boxes (32 rows x 32 fp32,
+        // 128-byte swizzle) that lane 0 hands to the TMA unit: a plain store
+        // (accumulate == 0) or a reduction that adds the box into the main
+        // grad at L2 (accumulate == 1), one add per element, so repeated calls
+        // are bitwise identical and no old value passes through the SM.
+        constexpr int WBOX = 32 * 128;
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        uint8_t* ring = c.out + (warp - 4) * 2 * WBOX;
+        const uint32_t ring_addr = ptx::smem_addr(ring);
+        int64_t tiles_done = 0, boxes = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+            if (t.skip)
+                continue;
+            uint32_t v[4][32];
+            if (t.nk > 0) {
+                if (!ptx::mbar_wait_warp(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
+                    break;
+                ptx::tc_fence_after_sync();
+                const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    ptx::tmem_wait_ld(v[cc]);
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(&c.tempty[0]);
+                ++tiles_done;
+            } else {                                      // empty group: dW_g = 0
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[cc][i] = 0u;
+            }
+            const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q);
+            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
+#pragma unroll
+            for (int b = 0; b < 4; ++b, ++boxes) {
+                const uint32_t slot = (uint32_t)(boxes & 1);
+                if (lane == 0)                            // the store two boxes back read this slot
+                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ptx::sts128(ring_addr + slot * WBOX + ptx::swz128(lane, j),
+                                make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (p.accumulate)
+                        ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
+                    else
+                        ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
+                    ptx::bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0)
+            ptx::bulk_wait_all();
     } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
         // ------------------------------------------------ wgrad epilogue --
         // The tile's fp32 result leaves through 128 x 32 boxes in shared
@@ -546,7 +615,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
             if (t.skip || t.nk == 0)
                 continue;
-            if (!ptx::mbar_wait(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
+            if (!ptx::mbar_wait_warp(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
                 break;
             ptx::tc_fence_after_sync();
             uint32_t v[4][32];
@@ -1285,9 +1354,10 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
         if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
         CUtensorMap mo;
-        if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, 128))
+        const bool wide = kWideTiles && k % 256 == 0;    // 32-row boxes per warp, else 128-row boxes
+        if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, wide ? 32 : 128))
             return GQ_ERR_CUDA;
-        if (kWideTiles && k % 256 == 0) {
+        if (wide) {
             const int64_t bound = (int64_t)G * (n / 128) * (k / 256);
             return run_mx<GEMM_WGRAD_MX, 256, false>(ma, mb, mo, args, bound, stream);
         }

@@ -91,6 +91,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait for a whole warp: lane 0 polls, the other lanes take its answer,
+// so that the warp stays converged for the warp-wide instructions after it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               int32_t* status)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)

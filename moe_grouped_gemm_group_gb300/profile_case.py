@@ -16,6 +16,11 @@ larger than the 129 MB L2):
   fprop2      moe_e64_zipf fc2 fprop (n 7168, k 2048, bf16 output)
   dgrad2      moe_e64_zipf fc2 dgrad (bf16 output)
   wgrad       moe_e8 fc1 k-grouped wgrad accumulating into fp32 (8 x 2048 x 4096)
+  wgrad64     moe_e64_zipf fc1 k-grouped wgrad accumulating into fp32
+              (64 x 2048 x 7168; 3.8 GB main grad)
+Options: --uniform replaces the workload's splits by the uniform split of
+the same live total; --store writes the wgrad result (accumulate = 0)
+instead of adding it to the main grad.
   wgrad_ch    kgrouped_zero_channel per-channel wgrad (4 x 2048 x 2048)
 Prints the mean CUDA-event time per launch.
 """
@@ -32,8 +37,11 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad_ch"])
+    ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad64",
+                                     "wgrad_ch"])
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--uniform", action="store_true")
+    ap.add_argument("--store", action="store_true")
     args = ap.parse_args()
 
     import numpy as np
@@ -49,7 +57,10 @@ def main():
     name = "moe_e8" if args.case == "wgrad" else "moe_e64_zipf"
     w = W.workload(name)
     E, H, F, R = w.num_groups, w.hidden, w.ffn, w.rows_cap
-    sp = torch.as_tensor(w.splits).to(dev)
+    splits = np.asarray(w.splits, np.int32)
+    if args.uniform:
+        splits = np.full(E, int(splits.sum()) // E, np.int32)
+    sp = torch.as_tensor(splits).to(dev)
 
     def quant(t, splits):
         q = gq.alloc_quantized(t.shape[0], t.shape[1], E, mx, dev)
@@ -74,11 +85,12 @@ def main():
             qd = quant(W.device_activation(w, n, 2, device=dev), sp)
             dx = torch.empty((R, k), dtype=torch.bfloat16, device=dev)
             fn = lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, n, k, dx, gq.DTYPE_BF16, st)  # noqa: E731
-    elif args.case == "wgrad":
+    elif args.case in ("wgrad", "wgrad64"):
         qx = quant(W.device_activation(w, H, 0, device=dev), sp)
         qd = quant(W.device_activation(w, F, 2, device=dev), sp)
         dw = W.device_normal_bf16((E, F, H), w.seed, 1e-3, 20, dev).float()
-        fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, True, st)  # noqa: E731
+        acc = not args.store
+        fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, acc, st)  # noqa: E731
     else:
         cw = W.workload("kgrouped_zero_channel")
         dyc, xc = W.kgrouped_zero_channel_operands(cw)
