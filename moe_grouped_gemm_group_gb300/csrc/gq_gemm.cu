@@ -48,6 +48,13 @@ constexpr int BM = 128;     // MMA M (rows of the A side)
 // L2 prefetch distance of the producers, in k-tiles (tuning knob; 0 = off):
 // the operand boxes of k-tile kt + PF are prefetched into L2 when k-tile kt
 // is loaded, so that first-touch DRAM latency hides behind the smem ring.
+// How the wide wgrad adds into the main grad (tuning knob): 1 = TMA load
+// of the old box, add in registers, TMA store; 0 = TMA reduce-add at L2.
+#ifndef GQ_WG_RMW
+#define GQ_WG_RMW 1
+#endif
+constexpr bool kWgLoadAddStore = GQ_WG_RMW != 0;
+
 #ifndef GQ_PF_DIST
 #define GQ_PF_DIST 0
 #endif
@@ -96,7 +103,10 @@ struct MxShape {
     static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales, slot 0
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 4 + (GQ_MAX_GROUPS + 2) * 4 + 8 + 32 * 8 + 32 * 4;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1) + 16;
+    // wide wgrad: one barrier per output box slot (8 warps x 2) for the TMA
+    // loads of the old main grad
+    static constexpr int OUT_BARS = (KIND == GEMM_WGRAD_MX && BN == 256) ? 16 : 0;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1 + OUT_BARS) + 16;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - OUT_BYTES - SCAN_BYTES - BAR_BYTES) / STAGE;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
@@ -117,6 +127,7 @@ struct Carve {
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
+    uint64_t* obar;       // output-box load barriers (wide wgrad)
     uint32_t* tmem_base;
     volatile int* abort;
     int32_t* s_off;       // group row offsets (rows_cap < 2^31 on every GEMM call)
@@ -126,7 +137,8 @@ struct Carve {
 };
 
 __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, int b_bytes,
-                                       int sfa_bytes, int sfb_bytes, int acc, int out_bytes = 0)
+                                       int sfa_bytes, int sfb_bytes, int acc, int out_bytes = 0,
+                                       int out_bars = 0)
 {
     Carve c;
     uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
@@ -147,7 +159,8 @@ __device__ __forceinline__ Carve carve(uint8_t* raw, int stages, int a_bytes, in
     c.tfull = c.empty + 8;
     c.tempty = c.tfull + acc;
     c.drain = c.tempty + acc;
-    c.tmem_base = reinterpret_cast<uint32_t*>(c.drain + 1);
+    c.obar = c.drain + 1;
+    c.tmem_base = reinterpret_cast<uint32_t*>(c.obar + out_bars);
     c.abort = reinterpret_cast<volatile int*>(c.tmem_base + 1);
     c.s_off = reinterpret_cast<int32_t*>(c.tmem_base + 4);
     c.s_tp = c.s_off + GQ_MAX_GROUPS + 1;
@@ -267,7 +280,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     constexpr bool B_MN = (KIND != GEMM_FPROP);
     extern __shared__ uint8_t smem_raw[];
     const Carve c = carve(smem_raw, S::STAGES, S::A_BYTES, S::B_BYTES, S::SFA_BYTES, S::SFB_BYTES,
-                          S::ACC, S::OUT_BYTES);
+                          S::ACC, S::OUT_BYTES, S::OUT_BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (load_status(p.status) != 0)
@@ -289,6 +302,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::mbar_init(&c.tempty[a], S::EPI_WARPS);
         }
         ptx::mbar_init(c.drain, 1);
+        for (int b = 0; b < S::OUT_BARS; ++b)
+            ptx::mbar_init(&c.obar[b], 1);
         *c.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -447,19 +462,41 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // to the main grad: the next tile's MMAs overlap this tile's memory
         // traffic, which is what bounds the k-grouped wgrad.  Each warp then
         // sends its rows through a ring of two 4 KB boxes (32 rows x 32 fp32,
-        // 128-byte swizzle) that lane 0 hands to the TMA unit: a plain store
-        // (accumulate == 0) or a reduction that adds the box into the main
-        // grad at L2 (accumulate == 1), one add per element, so repeated calls
-        // are bitwise identical and no old value passes through the SM.
+        // 128-byte swizzle) that lane 0 hands to the TMA unit.
+        //   accumulate == 0: plain TMA stores.
+        //   accumulate == 1: the old main-grad box comes in by TMA load (the
+        //     first two are issued before the accumulator is ready), the warp
+        //     adds its registers to it in place and TMA stores the sum.  (Or,
+        //     with the reduce-add form, the TMA unit adds the box at L2.)
+        //   Either way every element gets one round-to-nearest fp32 add, so
+        //   repeated calls are bitwise identical.
         constexpr int WBOX = 32 * 128;
-        const int q = warp & 3, h = (warp - 4) >> 2;
-        uint8_t* ring = c.out + (warp - 4) * 2 * WBOX;
+        const int q = warp & 3, h = (warp - 4) >> 2, w = warp - 4;
+        uint8_t* ring = c.out + w * 2 * WBOX;
         const uint32_t ring_addr = ptx::smem_addr(ring);
+        uint64_t* lbar = c.obar + 2 * w;                  // load barrier of each slot
+        // box k (counted over the whole call) uses slot k & 1, and its load
+        // is the (k >> 1)-th completion of that slot's barrier
+        int64_t loads = 0;
+        const bool rmw = kWgLoadAddStore && p.accumulate;
         int64_t tiles_done = 0, boxes = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
+        bool stop = false;
+        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort && !stop; tile += gridDim.x) {
             const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
             if (t.skip)
                 continue;
+            const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q);
+            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
+            if (rmw && lane == 0) {
+                // boxes 0 and 1 of this tile: both slots, once their last
+                // stores have read them
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                for (int b = 0; b < 2; ++b, ++loads) {
+                    const int slot = (int)(loads & 1);
+                    ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
+                    ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * b, orow);
+                }
+            }
             uint32_t v[4][32];
             if (t.nk > 0) {
                 if (!ptx::mbar_wait_warp(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
@@ -484,31 +521,59 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     for (int i = 0; i < 32; ++i)
                         v[cc][i] = 0u;
             }
-            const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q);
-            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
 #pragma unroll
             for (int b = 0; b < 4; ++b, ++boxes) {
-                const uint32_t slot = (uint32_t)(boxes & 1);
-                if (lane == 0)                            // the store two boxes back read this slot
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                __syncwarp();
+                const int slot = (int)(boxes & 1);
+                const uint32_t box = ring_addr + slot * WBOX;
+                if (rmw) {
+                    if (!ptx::mbar_wait_warp(&lbar[slot], (uint32_t)((boxes >> 1) & 1), c.abort, p.status)) {
+                        stop = true;
+                        break;
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ptx::sts128(ring_addr + slot * WBOX + ptx::swz128(lane, j),
-                                make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 o = ptx::lds128(box + ptx::swz128(lane, j));
+                        ptx::sts128(box + ptx::swz128(lane, j),
+                                    make_uint4(__float_as_uint(__uint_as_float(o.x) + __uint_as_float(v[b][4 * j])),
+                                               __float_as_uint(__uint_as_float(o.y) + __uint_as_float(v[b][4 * j + 1])),
+                                               __float_as_uint(__uint_as_float(o.z) + __uint_as_float(v[b][4 * j + 2])),
+                                               __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * j + 3]))));
+                    }
+                } else {
+                    if (lane == 0)                        // the store two boxes back read this slot
+                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::sts128(box + ptx::swz128(lane, j),
+                                    make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (p.accumulate)
+                    if (p.accumulate && !rmw)
                         ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
                     else
                         ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
                     ptx::bulk_commit_group();
+                    if (rmw && b + 2 < 4) {
+                        // box b + 2 into this slot once the store has read it
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
+                        ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * (b + 2), orow);
+                        ++loads;
+                    }
                 }
             }
         }
-        if (lane == 0)
+        if (lane == 0) {
+            // loads still in flight (an abort) land before the CTA leaves
+            volatile int no_abort = 0;
+            for (int64_t k = boxes; k < loads; ++k)
+                if (!ptx::mbar_wait(&lbar[k & 1], (uint32_t)((k >> 1) & 1), &no_abort, p.status))
+                    break;
             ptx::bulk_wait_all();
+        }
     } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
         // ------------------------------------------------ wgrad epilogue --
         // The tile's fp32 result leaves through 128 x 32 boxes in shared
