@@ -98,6 +98,12 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def job_value(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest
+    rank's time (`ms`, already the max over ranks), per second."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 # --------------------------------------------------------------------------- #
 # clocks sampled during the timed region                                      #
 # --------------------------------------------------------------------------- #
@@ -428,7 +434,7 @@ def main():
     ms_step = ms_total / args.steps
     if int(step.status.item()) != 0:
         raise SystemExit(f"device status {int(step.status.item())} in the timed region")
-    value = step.gemm_flops * dist.world / (ms_step * 1e-3) / 1e12
+    value = job_value(step.gemm_flops, dist.world, ms_step) / 1e12
     rows = summarize(step, events, peaks, peak_kind)
     dom = max(rows, key=lambda k: rows[k]["ms"] * rows[k]["launches"])
     d = rows[dom]
@@ -457,7 +463,7 @@ def main():
         e_ms = dist.max(a.elapsed_time(b)) / args.e2e_steps
         if int(step.h_status.item()) != 0:
             raise SystemExit("device status set in the e2e region")
-        e2e = {"value": round(step.gemm_flops * dist.world / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        e2e = {"value": round(job_value(step.gemm_flops, dist.world, e_ms) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h)}
 

@@ -9,13 +9,15 @@
 //
 // Work unit: a 128-row x 128-column tile that never straddles two groups
 // (groups are scanned in shared memory by every CTA; row tiles are numbered
-// group by group).  512 threads = 16 warps; warp (rb, cb) owns the 32 x 32
-// sub-block rows [32 rb, 32 rb + 32) x columns [32 cb, 32 cb + 32); lane l
-// holds row 32 rb + l of it in 16 registers (32 bf16).  A rowwise block is
-// one lane's 32 values (amax in registers); a columnwise block is one column
-// of the sub-block (amax by a warp-wide redux.sync).  One 128 x 128 tile
-// yields exactly one rowwise and one columnwise 512-byte scale atom, staged
-// in shared memory and written with 16-byte stores.
+// group by group).  k_quant_mx runs 16 consumer warps and one producer warp
+// that feeds a ring of input tiles by TMA.  Consumer warp (rb, cb) owns the
+// 32 x 32 sub-block rows [32 rb, 32 rb + 32) x columns [32 cb, 32 cb + 32);
+// lane l holds row 32 rb + l of it in 16 registers (32 bf16).  A rowwise
+// block is one lane's 32 values (amax in registers); a columnwise block is one
+// column of the sub-block (amax by a warp butterfly that leaves column j's
+// amax in lane j).  One 128 x 128 tile yields exactly one rowwise and one
+// columnwise 512-byte scale atom.  Codes and atoms are staged in swizzled
+// shared memory and leave by TMA stores and bulk copies.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
