@@ -25,6 +25,7 @@ than the 129 MB L2, so no L2 flush is needed between steps.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -41,6 +42,46 @@ if ROOT not in sys.path:
 METRIC = "grouped FP8 GEMM TFLOP/s + quantize GB/s on 1 GB300, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MXFP8_OVER_BF16 = 2.0      # nominal dense ratio: 4.5 vs 2.25 PFLOP/s
+
+# DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)
+# is measured once on this step and kept in a table under profiles/, each row
+# with a digest of the kernel sources it was taken on; a row whose sources
+# have changed since reads as unknown.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_moe_e64_zipf_step.md")
+KERNEL_SOURCES = {
+    "gemm": ["gq_gemm.cu", "gq_ptx.cuh", "gq_device.cuh", "gq_internal.h", "gq_host.cu"],
+    "quant": ["gq_quant.cu", "gq_ptx.cuh", "gq_device.cuh", "gq_internal.h", "gq_host.cu"],
+}
+
+
+def source_digest(family: str) -> str:
+    """First 16 hex digits of the sha256 of the family's kernel sources."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[family]:
+        with open(os.path.join(ROOT, "moe_grouped_gemm_group_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(name: str, kind: str):
+    """DRAM bytes per launch of launch `name` from the traffic table, or None
+    when the table has no row for it or the row's digest is stale."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            lines = fh.read().splitlines()
+    except OSError:
+        return None
+    want = source_digest("quant" if kind == "q" else "gemm")
+    for line in lines:
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 6 and cells[0] == name:
+            if cells[2] != want:
+                return None
+            try:
+                return int(cells[5])
+            except ValueError:
+                return None
+    return None
 
 
 def parse_args():
@@ -334,6 +375,7 @@ def summarize(step, events, peaks, peak_kind):
                 r.update(bound="tensor", achieved=round(tfs, 1), unit="TFLOP/s", peak=round(tc_burst, 1),
                          frac=round(tfs / tc_burst, 4), frac_of_sustained=round(tfs / tc_sus, 4),
                          algorithmic=flops)
+        r["traffic"] = measured_traffic(name, kind)
         rows[name] = r
     return rows
 
@@ -439,7 +481,7 @@ def main():
     dom = max(rows, key=lambda k: rows[k]["ms"] * rows[k]["launches"])
     d = rows[dom]
     roof = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
-            "unit": d["unit"], "frac": d["frac"], "traffic": None,
+            "unit": d["unit"], "frac": d["frac"], "traffic": d["traffic"],
             "peak_source": f"{peak_kind} ({'hbm_gbs' if d['bound'] == 'hbm' else 'bf16_tflops x 2 (MXFP8/bf16 nominal ratio)'})"}
     qbytes = sum(u for n, k, _, u in step.launches if k == "q")
     qms = sum(rows[n]["ms"] for n, k, _, _ in step.launches if k == "q")
