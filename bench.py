@@ -236,6 +236,8 @@ class Step:
         }
         self.splits = torch.as_tensor(wl.splits).to(device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # the wgrads' tile-claim workspace (one stream: the calls never overlap)
+        self.ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
         self.q = {
             "x1": gq.alloc_quantized(R, H, E, mx, device), "x2": gq.alloc_quantized(R, F, E, mx, device),
             "dy1": gq.alloc_quantized(R, F, E, mx, device), "dy2": gq.alloc_quantized(R, H, E, mx, device),
@@ -282,12 +284,14 @@ class Step:
             ("quant_dy2", "q", lambda: gq.gq_quantize(i["dy2"], sp, E, mx, q["dy2"], st), 4.0625 * L * H),
             ("dgrad2", "g", lambda: gq.gq_gemm_dgrad(q["dy2"], q["w2"], sp, E, H, F, o["dx2"], bf16, st),
              (2.0 * L * H * F, None)),
-            ("wgrad2", "g", lambda: gq.gq_gemm_wgrad(q["dy2"], q["x2"], sp, E, H, F, o["dw2"], True, st),
+            ("wgrad2", "g", lambda: gq.gq_gemm_wgrad(q["dy2"], q["x2"], sp, E, H, F, o["dw2"], True, st,
+                                                     workspace=self.ws),
              (2.0 * L * H * F, L * (H + F) * (1 + 1 / 32) + live_groups * H * F * 8.0)),
             ("quant_dy1", "q", lambda: gq.gq_quantize(i["dy1"], sp, E, mx, q["dy1"], st), 4.0625 * L * F),
             ("dgrad1", "g", lambda: gq.gq_gemm_dgrad(q["dy1"], q["w1"], sp, E, F, H, o["dx1"], bf16, st),
              (2.0 * L * F * H, None)),
-            ("wgrad1", "g", lambda: gq.gq_gemm_wgrad(q["dy1"], q["x1"], sp, E, F, H, o["dw1"], True, st),
+            ("wgrad1", "g", lambda: gq.gq_gemm_wgrad(q["dy1"], q["x1"], sp, E, F, H, o["dw1"], True, st,
+                                                     workspace=self.ws),
              (2.0 * L * F * H, L * (H + F) * (1 + 1 / 32) + live_groups * F * H * 8.0)),
             ("quant_ch_dy", "q", lambda: gq.gq_quantize(self.cin["dy"], self.csplits, 4, self.ch,
                                                          self.cq["dy"], st), (3 + 4 / 128) * cl * cw.hidden),

@@ -206,12 +206,28 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
  *           accumulate_into_main_grad of TransformerEngine issue 3484); an
  *           empty group then leaves dW_g bit-unchanged, with accumulate = 0
  *           it writes +0.0.
+ *   d_workspace : NULL, or caller-owned device memory of at least
+ *           GQ_WGRAD_WORKSPACE_BYTES bytes, 16-byte aligned, that the call
+ *           clears on `stream` before its kernel (cudaMemsetAsync) and uses
+ *           as tile-claim counters.  With a workspace the MX wgrad hands out
+ *           its output tiles at run time: half of the CTAs take tiles of the
+ *           groups in decreasing order of m_g, the other half in increasing
+ *           order, until the two meet, so the long contractions of the
+ *           largest groups overlap the main-grad traffic of the smallest
+ *           (with skewed splits every CTA would otherwise work through the
+ *           same group at the same time).  NULL keeps a static round-robin
+ *           order.  Two calls that may run at the same time must not share a
+ *           workspace.  The per-channel recipe ignores it.
+ *   workspace_bytes : size of d_workspace (ignored when it is NULL).
  * Deterministic: every output element is produced by one CTA in a fixed
- * order; repeated calls give bitwise identical results.
+ * order of additions, whichever CTA that is; repeated calls, with or without
+ * a workspace, give bitwise identical results.
  */
+#define GQ_WGRAD_WORKSPACE_BYTES 256
 gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
                         const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
-                        float* dw, int32_t accumulate, int32_t* d_status, gq_stream_t stream);
+                        float* dw, int32_t accumulate, void* d_workspace, uint64_t workspace_bytes,
+                        int32_t* d_status, gq_stream_t stream);
 
 #ifdef __cplusplus
 }

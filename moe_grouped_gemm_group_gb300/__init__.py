@@ -85,7 +85,7 @@ def load():
             f.restype = i32
             f.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         lib.gq_gemm_wgrad.restype = i32
-        lib.gq_gemm_wgrad.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
+        lib.gq_gemm_wgrad.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, C.c_uint64, vp, vp]
         _lib = lib
         return lib
 
@@ -233,9 +233,21 @@ def gq_gemm_dgrad(dy: GroupedTensor, w: GroupedTensor, splits, num_groups: int, 
     _check(st, "gq_gemm_dgrad")
 
 
+WGRAD_WORKSPACE_BYTES = 256       # GQ_WGRAD_WORKSPACE_BYTES
+
+
 def gq_gemm_wgrad(dy: GroupedTensor, x: GroupedTensor, splits, num_groups: int, n: int, k: int,
-                  dw, accumulate: bool, status, stream=None) -> None:
+                  dw, accumulate: bool, status, stream=None, workspace="new") -> None:
+    """`workspace`: a CUDA uint8 tensor of at least WGRAD_WORKSPACE_BYTES
+    bytes (run-time tile order; not shared by calls that may overlap), None
+    for the static order, or "new" (default) for a fresh one from torch's
+    allocator on dw's device."""
+    if isinstance(workspace, str):
+        import torch
+        workspace = torch.empty(WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=dw.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().gq_gemm_wgrad(C.byref(dy.desc), C.byref(x.desc), _ptr(splits, "splits", False),
                               num_groups, n, k, _ptr(dw, "dw"), int(bool(accumulate)),
+                              _ptr(workspace, "workspace", False), ws_bytes,
                               _ptr(status, "status"), _stream(stream))
     _check(st, "gq_gemm_wgrad")

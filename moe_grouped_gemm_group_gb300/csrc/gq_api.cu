@@ -265,7 +265,8 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
 
 gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
                         const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
-                        float* dw, int32_t accumulate, int32_t* d_status, gq_stream_t stream)
+                        float* dw, int32_t accumulate, void* d_workspace, uint64_t workspace_bytes,
+                        int32_t* d_status, gq_stream_t stream)
 {
     if (!dy || !x)
         return GQ_ERR_INVALID_ARG;
@@ -274,6 +275,10 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
         return st;
     if (accumulate != 0 && accumulate != 1)
         return GQ_ERR_INVALID_ARG;
+    if (d_workspace && workspace_bytes < GQ_WGRAD_WORKSPACE_BYTES)
+        return GQ_ERR_INVALID_ARG;
+    if (d_workspace && !aligned16(d_workspace))
+        return GQ_ERR_ALIGNMENT;
     if (dy->recipe.kind != x->recipe.kind)
         return GQ_ERR_UNSUPPORTED;
     const int32_t kind = dy->recipe.kind;
@@ -289,7 +294,7 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
                                                         : gq::GEMM_WGRAD_CHANNEL,
                            operand(dy, true), operand(x, true), d_split_sizes, num_groups,
                            dy->rows_cap, n, k, dw, GQ_DTYPE_F32, accumulate, d_status,
-                           (cudaStream_t)stream);
+                           (cudaStream_t)stream, d_workspace);
 }
 
 }  // extern "C"

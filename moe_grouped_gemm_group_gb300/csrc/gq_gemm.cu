@@ -48,12 +48,15 @@ constexpr int BM = 128;     // MMA M (rows of the A side)
 // L2 prefetch distance of the producers, in k-tiles (tuning knob; 0 = off):
 // the operand boxes of k-tile kt + PF are prefetched into L2 when k-tile kt
 // is loaded, so that first-touch DRAM latency hides behind the smem ring.
-// How the wide wgrad adds into the main grad (tuning knob): 1 = TMA load
-// of the old box, add in registers, TMA store; 0 = TMA reduce-add at L2.
-#ifndef GQ_WG_RMW
-#define GQ_WG_RMW 1
+// How the wide wgrad adds a tile into the main grad (tuning knob): tiles of
+// at least GQ_WG_RMW_MIN_K k-tiles load the old boxes by TMA, add in
+// registers and TMA-store the sums; shorter tiles hand their boxes to TMA
+// reduce-adds at L2 (0 = always load + add + store; a large value = always
+// reduce-add).
+#ifndef GQ_WG_RMW_MIN_K
+#define GQ_WG_RMW_MIN_K 4
 #endif
-constexpr bool kWgLoadAddStore = GQ_WG_RMW != 0;
+constexpr int kWgRmwMinK = GQ_WG_RMW_MIN_K;
 
 #ifndef GQ_PF_DIST
 #define GQ_PF_DIST 0
@@ -73,7 +76,24 @@ struct GemmArgs {
     void* out;
     int accumulate;
     int32_t* status;
+    // k-grouped MX wgrad only: tile-claim counter (low 32 bits: tiles taken
+    // from the front of the run-time order, high 32 bits: from the back), or
+    // null for the static round-robin order; CTAs below front_ctas claim
+    // from the front
+    unsigned long long* claim = nullptr;
+    int front_ctas = 0;
 };
+
+// x-operand bytes of a group above which the wgrad walks its tiles column by
+// column (see decode_tile).
+#ifndef GQ_WG_COLUMN_ORDER_MB
+#define GQ_WG_COLUMN_ORDER_MB 32
+#endif
+constexpr int64_t kWgColumnOrderBytes = (int64_t)GQ_WG_COLUMN_ORDER_MB << 20;
+
+// Depth of the shared-memory ring through which the producer passes claimed
+// tiles to the MMA issuer and the epilogue warps.
+constexpr int kTileRing = 8;
 
 template <int KIND, int BN>
 struct MxShape {
@@ -102,11 +122,15 @@ struct MxShape {
     static constexpr uint32_t SFA_COL = ACC * BN;                     // TMEM column of A scales, slot 0
     static constexpr uint32_t SFB_COL = SFA_COL + 4;                  // TMEM column of B scales, slot 0
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 4 + (GQ_MAX_GROUPS + 2) * 4 + 8 + 32 * 8 + 32 * 4;
+    // wgrad adds the groups in decreasing order of size and the tile ring
+    static constexpr int SCAN_BYTES = (GQ_MAX_GROUPS + 1) * 4 + (GQ_MAX_GROUPS + 2) * 4 + 8 + 32 * 8 + 32 * 4 +
+                                      (KIND == GEMM_WGRAD_MX ? (GQ_MAX_GROUPS + kTileRing) * 4 : 0);
     // wide wgrad: one barrier per output box slot (8 warps x 2) for the TMA
     // loads of the old main grad
     static constexpr int OUT_BARS = (KIND == GEMM_WGRAD_MX && BN == 256) ? 16 : 0;
-    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1 + OUT_BARS) + 16;
+    // wgrad: full / empty barriers of the claimed-tile ring
+    static constexpr int RING_BARS = KIND == GEMM_WGRAD_MX ? 2 * kTileRing : 0;
+    static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1 + OUT_BARS + RING_BARS) + 16;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - OUT_BYTES - SCAN_BYTES - BAR_BYTES) / STAGE;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
@@ -195,7 +219,8 @@ __device__ __forceinline__ int64_t tile_count(const GemmArgs& p, const int32_t* 
 
 template <int KIND, int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& p, const int32_t* s_off,
-                                            const int32_t* s_tp, int64_t tile)
+                                            const int32_t* s_tp, int64_t tile,
+                                            const int32_t* ord = nullptr)
 {
     Tile t;
     if (KIND == GEMM_FPROP || KIND == GEMM_DGRAD) {
@@ -215,11 +240,24 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& p, const int32_t* s_
     } else {
         const int64_t nkt = p.k / BN;
         const int64_t per_group = (p.n / BM) * nkt;
-        t.g = (int)(tile / per_group);
-        const int64_t rem = tile - (int64_t)t.g * per_group;
-        t.mt = rem / nkt;
-        t.col0 = (rem - t.mt * nkt) * BN;
+        const int64_t gi = tile / per_group;              // position in the group order
+        t.g = ord ? ord[gi] : (int)gi;
+        const int64_t rem = tile - gi * per_group;
         const int64_t m = s_off[t.g + 1] - s_off[t.g];
+        // Tiles running at the same time share operand columns through L2.
+        // By default they walk the output row by row (whole main-grad rows
+        // at a time), which re-reads the group's x columns once per wave of
+        // tiles; for a group whose x operand outgrows L2's share and is the
+        // larger of the two, they walk column by column instead, so that
+        // the smaller dy operand is the one read again.
+        if (p.k > p.n && m * p.k > kWgColumnOrderBytes) {
+            const int64_t nmt = p.n / BM;
+            t.mt = rem % nmt;
+            t.col0 = (rem / nmt) * BN;
+        } else {
+            t.mt = rem / nkt;
+            t.col0 = (rem - t.mt * nkt) * BN;
+        }
         t.row0 = s_off[t.g];
         t.rows = 128;
         t.nk = (int)((m + 127) / 128);
@@ -255,6 +293,55 @@ __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t (&r
     }
 }
 
+// One claim from the wgrad's tile-claim counter: the next tile from the front
+// (or back) of the run-time order, or -1 once the two ends have met.  Every
+// tile is handed out exactly once: a claim is granted only while the claims
+// granted so far, from both ends, number fewer than ntiles.
+__device__ __forceinline__ int64_t claim_tile(unsigned long long* claim, bool front, int64_t ntiles)
+{
+    const unsigned long long old = atomicAdd(claim, front ? 1ull : (1ull << 32));
+    const int64_t f = (int64_t)(old & 0xffffffffull), b = (int64_t)(old >> 32);
+    if (f + b >= ntiles)
+        return -1;
+    return front ? f : ntiles - 1 - b;
+}
+
+// Producer side of the claimed-tile ring: entry q gets `tile` (-1 ends the
+// sequence).  False if the wait for a free entry gave up.
+__device__ __forceinline__ bool ring_put(uint64_t* full, uint64_t* empty, int32_t* ring, int64_t& q,
+                                         int64_t tile, volatile int* abort, int32_t* status)
+{
+    const int e = (int)(q % kTileRing);
+    if (!ptx::mbar_wait(&empty[e], (uint32_t)(((q / kTileRing) & 1) ^ 1), abort, status))
+        return false;
+    *reinterpret_cast<volatile int32_t*>(&ring[e]) = (int32_t)tile;
+    ptx::mbar_arrive(&full[e]);
+    ++q;
+    return true;
+}
+
+// Consumer side: entry q of the ring, -1 at the end of the sequence or when
+// the wait gave up.  WARP: the whole warp calls it and gets the same value,
+// and one arrival per warp frees the entry.
+template <bool WARP>
+__device__ __forceinline__ int64_t ring_get(uint64_t* full, uint64_t* empty, const int32_t* ring, int64_t& q,
+                                            volatile int* abort, int32_t* status)
+{
+    const int e = (int)(q % kTileRing);
+    const uint32_t par = (uint32_t)((q / kTileRing) & 1);
+    const bool ok = WARP ? ptx::mbar_wait_warp(&full[e], par, abort, status)
+                         : ptx::mbar_wait(&full[e], par, abort, status);
+    if (!ok)
+        return -1;
+    const int64_t tile = *reinterpret_cast<const volatile int32_t*>(&ring[e]);
+    if (WARP)
+        __syncwarp();
+    if (!WARP || (threadIdx.x & 31) == 0)
+        ptx::mbar_arrive(&empty[e]);
+    ++q;
+    return tile;
+}
+
 // Wait for the TMA writes of the last min(stages, issued) issued stages, so
 // that none lands after the CTA has left (bounded; used on every exit path).
 __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t issued,
@@ -280,7 +367,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     constexpr bool B_MN = (KIND != GEMM_FPROP);
     extern __shared__ uint8_t smem_raw[];
     const Carve c = carve(smem_raw, S::STAGES, S::A_BYTES, S::B_BYTES, S::SFA_BYTES, S::SFB_BYTES,
-                          S::ACC, S::OUT_BYTES, S::OUT_BARS);
+                          S::ACC, S::OUT_BYTES, S::OUT_BARS + S::RING_BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (load_status(p.status) != 0)
@@ -304,6 +391,10 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         ptx::mbar_init(c.drain, 1);
         for (int b = 0; b < S::OUT_BARS; ++b)
             ptx::mbar_init(&c.obar[b], 1);
+        for (int b = 0; b < S::RING_BARS / 2; ++b) {
+            ptx::mbar_init(&c.obar[S::OUT_BARS + b], 1);                        // full
+            ptx::mbar_init(&c.obar[S::OUT_BARS + kTileRing + b], 1 + S::EPI_WARPS);  // empty
+        }
         *c.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -317,6 +408,26 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         if (KIND == GEMM_WGRAD_MX || BN == 256)
             ptx::prefetch_tmap(&tma_o);
     }
+    // k-grouped wgrad with a claim counter: tiles are handed out at run time,
+    // in the order of the groups sorted by decreasing size (ties by index);
+    // the producer claims and the other roles read the claims from the ring
+    const bool dyn = KIND == GEMM_WGRAD_MX && p.claim != nullptr;
+    int32_t* s_ord = c.s_w32 + 32;
+    int32_t* s_ring = s_ord + GQ_MAX_GROUPS;
+    uint64_t* ring_full = c.obar + S::OUT_BARS;
+    uint64_t* ring_empty = ring_full + kTileRing;
+    const int32_t* ord = dyn ? s_ord : nullptr;
+    if (dyn) {
+        for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+            const int32_t mg = c.s_off[g + 1] - c.s_off[g];
+            int r = 0;
+            for (int o = 0; o < p.G; ++o) {
+                const int32_t mo = c.s_off[o + 1] - c.s_off[o];
+                r += (mo > mg) || (mo == mg && o < g);
+            }
+            s_ord[r] = g;
+        }
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -325,9 +436,23 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer --
-        int64_t issued = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+        int64_t issued = 0, cursor = blockIdx.x, rq = 0;
+        const bool front = (int)blockIdx.x < p.front_ctas;
+        while (!*c.abort) {
+            int64_t tile;
+            if (!dyn) {
+                tile = cursor;
+                cursor += gridDim.x;
+                if (tile >= ntiles)
+                    break;
+            } else {
+                tile = claim_tile(p.claim, front, ntiles);
+                if (tile >= 0 && decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord).skip)
+                    continue;
+                if (!ring_put(ring_full, ring_empty, s_ring, rq, tile, c.abort, p.status) || tile < 0)
+                    break;
+            }
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord);
             if (t.skip || t.nk == 0)
                 continue;
             for (int kt = 0; kt < t.nk; ++kt, ++issued) {
@@ -403,9 +528,18 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         drain_loads(c.full, S::STAGES, issued, p.status);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------- MMA issuer --
-        int64_t consumed = 0, tiles_done = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort; tile += gridDim.x) {
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+        int64_t consumed = 0, tiles_done = 0, cursor = blockIdx.x, rq = 0;
+        while (!*c.abort) {
+            int64_t tile;
+            if (!dyn) {
+                tile = cursor;
+                cursor += gridDim.x;
+                if (tile >= ntiles)
+                    break;
+            } else if ((tile = ring_get<false>(ring_full, ring_empty, s_ring, rq, c.abort, p.status)) < 0) {
+                break;
+            }
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord);
             if (t.skip || t.nk == 0)
                 continue;
             const int acc = (int)(tiles_done % S::ACC);
@@ -464,10 +598,14 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // sends its rows through a ring of two 4 KB boxes (32 rows x 32 fp32,
         // 128-byte swizzle) that lane 0 hands to the TMA unit.
         //   accumulate == 0: plain TMA stores.
-        //   accumulate == 1: the old main-grad box comes in by TMA load (the
-        //     first two are issued before the accumulator is ready), the warp
-        //     adds its registers to it in place and TMA stores the sum.  (Or,
-        //     with the reduce-add form, the TMA unit adds the box at L2.)
+        //   accumulate == 1, a tile of at least kWgRmwMinK k-tiles: the old
+        //     main-grad box comes in by TMA load (the first two are issued
+        //     before the accumulator is ready), the warp adds its registers
+        //     to it in place and TMA-stores the sum.  Each warp has two boxes
+        //     in flight, so a CTA's main-grad bandwidth is bounded by the load
+        //     latency; a long contraction hides it.
+        //   accumulate == 1, a shorter tile: the TMA unit adds the box into
+        //     the main grad at L2 (reduce-add), which needs no load in flight.
         //   Either way every element gets one round-to-nearest fp32 add, so
         //   repeated calls are bitwise identical.
         constexpr int WBOX = 32 * 128;
@@ -475,26 +613,38 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         uint8_t* ring = c.out + w * 2 * WBOX;
         const uint32_t ring_addr = ptx::smem_addr(ring);
         uint64_t* lbar = c.obar + 2 * w;                  // load barrier of each slot
-        // box k (counted over the whole call) uses slot k & 1, and its load
-        // is the (k >> 1)-th completion of that slot's barrier
-        int64_t loads = 0;
-        const bool rmw = kWgLoadAddStore && p.accumulate;
+        // box k (counted over the whole call) uses slot k & 1; per slot, bit
+        // s of lph is the parity of its next load completion and bit s of
+        // lpend says whether a load into it is in flight (lane 0's copy)
+        uint32_t lph = 0u, lpend = 0u;
         int64_t tiles_done = 0, boxes = 0;
         bool stop = false;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !*c.abort && !stop; tile += gridDim.x) {
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+        int64_t cursor = blockIdx.x, rq = 0;
+        while (!*c.abort && !stop) {
+            int64_t tile;
+            if (!dyn) {
+                tile = cursor;
+                cursor += gridDim.x;
+                if (tile >= ntiles)
+                    break;
+            } else if ((tile = ring_get<true>(ring_full, ring_empty, s_ring, rq, c.abort, p.status)) < 0) {
+                break;
+            }
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord);
             if (t.skip)
                 continue;
             const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q);
             const int32_t ocol = (int32_t)(t.col0 + 128 * h);
+            const bool rmw = p.accumulate && t.nk >= kWgRmwMinK;
             if (rmw && lane == 0) {
                 // boxes 0 and 1 of this tile: both slots, once their last
                 // stores have read them
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                for (int b = 0; b < 2; ++b, ++loads) {
-                    const int slot = (int)(loads & 1);
+                for (int b = 0; b < 2; ++b) {
+                    const int slot = (int)((boxes + b) & 1);
                     ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
                     ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * b, orow);
+                    lpend |= 1u << slot;
                 }
             }
             uint32_t v[4][32];
@@ -526,10 +676,12 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 const int slot = (int)(boxes & 1);
                 const uint32_t box = ring_addr + slot * WBOX;
                 if (rmw) {
-                    if (!ptx::mbar_wait_warp(&lbar[slot], (uint32_t)((boxes >> 1) & 1), c.abort, p.status)) {
+                    if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
                         stop = true;
                         break;
                     }
+                    lph ^= 1u << slot;
+                    lpend &= ~(1u << slot);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint4 o = ptx::lds128(box + ptx::swz128(lane, j));
@@ -561,7 +713,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                         ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
                         ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * (b + 2), orow);
-                        ++loads;
+                        lpend |= 1u << slot;
                     }
                 }
             }
@@ -569,9 +721,9 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         if (lane == 0) {
             // loads still in flight (an abort) land before the CTA leaves
             volatile int no_abort = 0;
-            for (int64_t k = boxes; k < loads; ++k)
-                if (!ptx::mbar_wait(&lbar[k & 1], (uint32_t)((k >> 1) & 1), &no_abort, p.status))
-                    break;
+            for (int sl = 0; sl < 2; ++sl)
+                if ((lpend >> sl) & 1u)
+                    ptx::mbar_wait(&lbar[sl], (lph >> sl) & 1u, &no_abort, p.status);
             ptx::bulk_wait_all();
         }
     } else if (warp >= 4 && KIND == GEMM_WGRAD_MX) {
@@ -582,9 +734,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // store (accumulate == 0) or a reduction that adds it into the main
         // grad at L2 (accumulate == 1), one add per element, so repeated
         // calls are bitwise identical.  No old value passes through the SM.
-        // BN = 128: 4 warps, one ring of four boxes.  BN = 256: 8 warps in
-        // two halves of 128 columns, each with a ring of two boxes; halves
-        // meet on named barriers 1 and 2.
+        // 4 warps (BN = 128), one ring of four boxes; the warps meet on named
+        // barrier 1.
         constexpr int HALVES = S::EPI_WARPS / 4;
         constexpr int SLOTS = 4 / HALVES;                 // boxes per ring
         constexpr int BOX = BM * 128;
@@ -595,8 +746,21 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         uint8_t* ring = c.out + h * SLOTS * BOX;
         int64_t tiles_done = 0, q_proc = 0;
         bool stop = false;
-        for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile);
+        int64_t cursor = blockIdx.x, rq = 0;
+        while (!stop) {
+            int64_t tile;
+            if (!dyn) {
+                tile = cursor;
+                cursor += gridDim.x;
+                if (tile >= ntiles)
+                    break;
+            } else {
+                tile = ring_get<true>(ring_full, ring_empty, s_ring, rq, c.abort, p.status);
+                // every warp of the half reads the same entry; leave together
+                if (ptx::named_barrier_or(bar_id, 128, tile < 0))
+                    break;
+            }
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord);
             if (t.skip)
                 continue;
             const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM);
@@ -1298,7 +1462,9 @@ gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap
     if (prepare(kernel, S::SMEM) != cudaSuccess)
         return GQ_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
-    kernel<<<(unsigned)grid, S::THREADS, S::SMEM, stream>>>(ma, mb, mo, args);
+    GemmArgs a = args;
+    a.front_ctas = (int)(grid / 2);
+    kernel<<<(unsigned)grid, S::THREADS, S::SMEM, stream>>>(ma, mb, mo, a);
     return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 
@@ -1347,7 +1513,7 @@ bool make_scale_map(CUtensorMap* map, const void* base, uint64_t bytes)
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
-                      cudaStream_t stream)
+                      cudaStream_t stream, void* workspace)
 {
     GemmArgs args;
     args.splits = splits;
@@ -1420,6 +1586,13 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
             return GQ_ERR_CUDA;
         CUtensorMap mo;
         const bool wide = kWideTiles && k % 256 == 0;    // 32-row boxes per warp, else 128-row boxes
+        const int64_t ntiles = (int64_t)G * (n / 128) * (k / (wide ? 256 : 128));
+        if (workspace && ntiles < (int64_t(1) << 31)) {
+            // run-time tile order: the claim counter starts at zero
+            if (cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+                return GQ_ERR_CUDA;
+            args.claim = static_cast<unsigned long long*>(workspace);
+        }
         if (!make_tensor_map_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, (int64_t)G * n, k, 32, wide ? 32 : 128))
             return GQ_ERR_CUDA;
         if (wide) {

@@ -70,6 +70,6 @@ enum GemmKind { GEMM_FPROP = 0, GEMM_DGRAD = 1, GEMM_WGRAD_MX = 2, GEMM_WGRAD_CH
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
-                      cudaStream_t stream);
+                      cudaStream_t stream, void* workspace = nullptr);
 
 }  // namespace gq

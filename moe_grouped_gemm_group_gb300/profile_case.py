@@ -20,7 +20,8 @@ larger than the 129 MB L2):
               (64 x 2048 x 7168; 3.8 GB main grad)
 Options: --uniform replaces the workload's splits by the uniform split of
 the same live total; --store writes the wgrad result (accumulate = 0)
-instead of adding it to the main grad.
+instead of adding it to the main grad; --static runs the wgrad in its static
+tile order (no claim workspace).
   wgrad_ch    kgrouped_zero_channel per-channel wgrad (4 x 2048 x 2048)
 Prints the mean CUDA-event time per launch.
 """
@@ -42,6 +43,7 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--uniform", action="store_true")
     ap.add_argument("--store", action="store_true")
+    ap.add_argument("--static", action="store_true")
     args = ap.parse_args()
 
     import numpy as np
@@ -90,7 +92,8 @@ def main():
         qd = quant(W.device_activation(w, F, 2, device=dev), sp)
         dw = W.device_normal_bf16((E, F, H), w.seed, 1e-3, 20, dev).float()
         acc = not args.store
-        fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, acc, st)  # noqa: E731
+        ws = None if args.static else torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+        fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, acc, st, workspace=ws)  # noqa: E731
     else:
         cw = W.workload("kgrouped_zero_channel")
         dyc, xc = W.kgrouped_zero_channel_operands(cw)

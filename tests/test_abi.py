@@ -106,10 +106,15 @@ def test_gemm_host_checks_need_no_gpu(lib):
     dy.row_data, dy.row_scale, dy.row_scale_bytes = 0x40000, 0x50000, 1 << 20
     assert lib.gq_gemm_dgrad(C.byref(dy), C.byref(w), None, 1, 128, 256, out, 0, st, None) in (-4, -7)
     # wgrad needs columnwise operands, same recipe, accumulate in {0, 1}
-    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 0, st, None) in (-4, -7)
-    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 2, st, None) == -1
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 0, None, 0, st, None) in (-4, -7)
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 2, None, 0, st, None) == -1
     xc = _desc(1, 256, 256, kind=1, row=0, col=1)
-    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(xc), None, 1, 128, 256, out, 0, st, None) == -4
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(xc), None, 1, 128, 256, out, 0, None, 0, st, None) == -4
+    # a workspace smaller than GQ_WGRAD_WORKSPACE_BYTES, or not 16-byte aligned
+    ws = C.c_void_p(0x80000)
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 0, ws, 255, st, None) == -1
+    assert lib.gq_gemm_wgrad(C.byref(dy), C.byref(x), None, 1, 128, 256, out, 0, C.c_void_p(0x80008), 256,
+                             st, None) == -2
     # scale capacity below the bound
     x2 = _desc(1, 256, 256, row=1, col=0)
     x2.row_data, x2.row_scale, x2.row_scale_bytes = 0x40000, 0x50000, 16

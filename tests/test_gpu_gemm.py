@@ -69,7 +69,7 @@ def ora_dgrad(dy_bits, w_bits, splits, G, N, K):
                         O.quantize_mx(w_bits, None, G, rowwise=False), splits, G, N, K)
 
 
-def gpu_wgrad(dy_bits, x_bits, splits, G, N, K, accumulate=False, init=None, recipe=None):
+def gpu_wgrad(dy_bits, x_bits, splits, G, N, K, accumulate=False, init=None, recipe=None, workspace="new"):
     st = status_dev()
     recipe = recipe or mx_recipe(False, True)
     dyq, _ = quantize(dy_bits, splits, G, recipe, status=st)
@@ -78,7 +78,7 @@ def gpu_wgrad(dy_bits, x_bits, splits, G, N, K, accumulate=False, init=None, rec
         dw = torch.full((G, N, K), float("nan"), dtype=torch.float32, device=DEV)
     else:
         dw = torch.from_numpy(np.ascontiguousarray(init, np.float32)).to(DEV)
-    gq.gq_gemm_wgrad(dyq, xq, splits_dev(splits), G, N, K, dw, accumulate, st)
+    gq.gq_gemm_wgrad(dyq, xq, splits_dev(splits), G, N, K, dw, accumulate, st, workspace=workspace)
     check_status(st)
     return host(dw)
 
@@ -154,6 +154,35 @@ def test_wgrad_matches_oracle(splits, pad, N, K):
     got = gpu_wgrad(dy, x, splits, G, N, K)
     want = ora_wgrad(dy, x, splits, G, N, K)
     assert_groups_close(got, want, "wgrad")
+
+
+@pytest.mark.parametrize("K", [512, 384])
+def test_wgrad_run_time_order_matches_static_order(K):
+    """Skewed splits (one large group, empty and 32-row groups): the run-time
+    tile order (claim workspace; both ends of the size-sorted group list) and
+    the static order give the same bits, and match the oracle; a reused
+    workspace is cleared by every call."""
+    splits = np.array([32, 0, 1088, 96, 0, 32, 320, 64], np.int32)
+    G, L, N = len(splits), int(splits.sum()), 256
+    dy = np.concatenate([W.normal_bf16((L, N), 31), W.uniform_bf16((64, N), 32, -4, 4)])
+    x = np.concatenate([W.normal_bf16((L, K), 33), W.uniform_bf16((64, K), 34, -4, 4)])
+    init = W.bf16_bits_to_f32(W.normal_bf16((G, N, K), 35))
+    ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=DEV)
+    stat = gpu_wgrad(dy, x, splits, G, N, K, True, init, workspace=None)
+    dyn1 = gpu_wgrad(dy, x, splits, G, N, K, True, init, workspace=ws)
+    dyn2 = gpu_wgrad(dy, x, splits, G, N, K, True, init, workspace=ws)
+    assert np.array_equal(stat.view(np.uint32), dyn1.view(np.uint32))
+    assert np.array_equal(dyn1.view(np.uint32), dyn2.view(np.uint32))
+    want = ora_wgrad(dy, x, splits, G, N, K, True, init)
+    for g in range(G):
+        if splits[g] == 0:
+            assert np.array_equal(dyn1[g].view(np.uint32), init[g].view(np.uint32))
+    assert_groups_close(dyn1, want, "wgrad")
+    # accumulate = 0: empty groups are written as +0.0 in either order
+    z_stat = gpu_wgrad(dy, x, splits, G, N, K, False, None, workspace=None)
+    z_dyn = gpu_wgrad(dy, x, splits, G, N, K, False, None, workspace=ws)
+    assert np.array_equal(z_stat.view(np.uint32), z_dyn.view(np.uint32))
+    assert np.all(z_dyn[splits == 0] == 0)
 
 
 @pytest.mark.parametrize("kind,K", [("fprop", 384), ("dgrad", 384), ("fprop", 512), ("dgrad", 512)])
