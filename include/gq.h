@@ -229,6 +229,34 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
                         float* dw, int32_t accumulate, void* d_workspace, uint64_t workspace_bytes,
                         int32_t* d_status, gq_stream_t stream);
 
+/*
+ * gq_gemm_wgrad_noalloc -- gq_gemm_wgrad with the run-time tile order, for
+ * callers that cannot supply a workspace.  The pages describe no such call:
+ * it exists for hosts that have no device allocator of their own (a C or
+ * Fortran program linking only this library) or that must not allocate on
+ * this path (a cudaMalloc can wait for the whole device to go idle, and
+ * memory pools owned by a framework may not be reachable from here).
+ *
+ * It allocates nothing.  The workspace is a GQ_WGRAD_WORKSPACE_BYTES-byte
+ * array inside the library, one per device, held by every device that loads
+ * the library until the process exits.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress, with the device current)
+ * and keeps it; make that first call before any stream capture.  Each call
+ * clears the array's claim counter on `stream` before its kernel.  All calls
+ * on a device share the one array, so calls that may overlap on the GPU (on
+ * different streams without ordering between them) race and must not be
+ * issued; serialise them, or use gq_gemm_wgrad with one workspace per stream.
+ *
+ * Arguments, layouts, results and errors are those of gq_gemm_wgrad.  In
+ * addition, a problem of 2^31 or more output tiles (num_groups * n/128 *
+ * k/256, or k/128 when k % 256 != 0) exceeds the counter and returns
+ * GQ_ERR_INVALID_ARG before anything is launched.
+ */
+gq_status gq_gemm_wgrad_noalloc(const gq_quantized* dy, const gq_quantized* x,
+                                const int32_t* d_split_sizes, int32_t num_groups, int64_t n,
+                                int64_t k, float* dw, int32_t accumulate, int32_t* d_status,
+                                gq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

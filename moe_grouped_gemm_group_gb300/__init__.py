@@ -16,7 +16,7 @@ import threading
 __all__ = [
     "GQError", "Recipe", "Quantized", "GroupedTensor", "load", "library_path",
     "gq_status_string", "gq_version", "gq_scale_bytes_bound", "gq_split_scan", "gq_quantize",
-    "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "alloc_quantized",
+    "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_gemm_wgrad_noalloc", "alloc_quantized",
     "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "DTYPE_F32", "DTYPE_BF16", "STATUS",
 ]
 
@@ -86,6 +86,8 @@ def load():
             f.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         lib.gq_gemm_wgrad.restype = i32
         lib.gq_gemm_wgrad.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, C.c_uint64, vp, vp]
+        lib.gq_gemm_wgrad_noalloc.restype = i32
+        lib.gq_gemm_wgrad_noalloc.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         _lib = lib
         return lib
 
@@ -251,3 +253,14 @@ def gq_gemm_wgrad(dy: GroupedTensor, x: GroupedTensor, splits, num_groups: int, 
                               _ptr(workspace, "workspace", False), ws_bytes,
                               _ptr(status, "status"), _stream(stream))
     _check(st, "gq_gemm_wgrad")
+
+
+def gq_gemm_wgrad_noalloc(dy: GroupedTensor, x: GroupedTensor, splits, num_groups: int, n: int, k: int,
+                          dw, accumulate: bool, status, stream=None) -> None:
+    """gq_gemm_wgrad without a caller workspace: the library's own per-device
+    array serves as one (calls that may overlap on the GPU must not be
+    issued; see include/gq.h)."""
+    st = load().gq_gemm_wgrad_noalloc(C.byref(dy.desc), C.byref(x.desc), _ptr(splits, "splits", False),
+                                      num_groups, n, k, _ptr(dw, "dw"), int(bool(accumulate)),
+                                      _ptr(status, "status"), _stream(stream))
+    _check(st, "gq_gemm_wgrad_noalloc")

@@ -121,6 +121,11 @@ def test_gemm_host_checks_need_no_gpu(lib):
     assert lib.gq_gemm_fprop(C.byref(x2), C.byref(w), None, 1, 128, 256, out, 0, st, None) == -1
 
 
+def test_noalloc_wgrad_refuses_too_many_tiles_without_a_gpu(lib):
+    # 2^31 output tiles exceed the claim counter: refused on the host
+    assert lib.gq_gemm_wgrad_noalloc(None, None, None, 1024, 1 << 17, 1 << 19, None, 1, None, None) == -1
+
+
 def test_binding_refuses_host_tensors(lib):
     torch = pytest.importorskip("torch")
     x = torch.zeros((128, 128), dtype=torch.bfloat16)
