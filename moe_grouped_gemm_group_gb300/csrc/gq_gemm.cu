@@ -84,6 +84,22 @@ struct GemmArgs {
     int front_ctas = 0;
 };
 
+// Output box slots per epilogue warp of the wide wgrad (tuning knob): more
+// slots keep more of the old main grad in flight per CTA but leave room for
+// fewer pipeline stages.
+#ifndef GQ_WG_SLOTS
+#define GQ_WG_SLOTS 2
+#endif
+constexpr int kWgSlots = GQ_WG_SLOTS;
+
+// Share of the wgrad's CTAs (percent) that claim tiles from the largest
+// groups down in the run-time order; the others start from the smallest
+// (tuning knob).
+#ifndef GQ_WG_FRONT_PCT
+#define GQ_WG_FRONT_PCT 50
+#endif
+constexpr int kWgFrontPct = GQ_WG_FRONT_PCT;
+
 // x-operand bytes of a group above which the wgrad walks its tiles column by
 // column (see decode_tile).
 #ifndef GQ_WG_COLUMN_ORDER_MB
@@ -108,10 +124,11 @@ struct MxShape {
     static constexpr int STAGE = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     // wgrad sends its fp32 output through 64 KB of shared memory on the way
     // to a TMA store or reduce-add: a ring of four 128 x 32 boxes for
-    // BN = 128, a ring of two 32 x 32 boxes per epilogue warp for BN = 256.
-    // fprop/dgrad with BN = 256 stage their output too: each of the 8
-    // epilogue warps owns a 2 KB box of 32 rows x 64 bytes (64-byte swizzle).
-    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? 4 * BM * 128
+    // BN = 128, a ring of kWgSlots 32 x 32 boxes per epilogue warp for
+    // BN = 256.  fprop/dgrad with BN = 256 stage their output too: each of
+    // the 8 epilogue warps owns a 2 KB box of 32 rows x 64 bytes (64-byte
+    // swizzle).
+    static constexpr int OUT_BYTES = KIND == GEMM_WGRAD_MX ? (BN == 256 ? 8 * kWgSlots * 32 * 128 : 4 * BM * 128)
                                      : (BN == 256 ? kEpiBox * 8 : 0);
     static constexpr int ACC = BN == 128 ? 2 : 1;                    // TMEM accumulator buffers
     // Scale factors rotate through SF_SLOTS column groups, so that the copy
@@ -127,7 +144,7 @@ struct MxShape {
                                       (KIND == GEMM_WGRAD_MX ? (GQ_MAX_GROUPS + kTileRing) * 4 : 0);
     // wide wgrad: one barrier per output box slot (8 warps x 2) for the TMA
     // loads of the old main grad
-    static constexpr int OUT_BARS = (KIND == GEMM_WGRAD_MX && BN == 256) ? 16 : 0;
+    static constexpr int OUT_BARS = (KIND == GEMM_WGRAD_MX && BN == 256) ? 8 * kWgSlots : 0;
     // wgrad: full / empty barriers of the claimed-tile ring
     static constexpr int RING_BARS = KIND == GEMM_WGRAD_MX ? 2 * kTileRing : 0;
     static constexpr int BAR_BYTES = 8 * (2 * 8 + 2 * ACC + 1 + OUT_BARS + RING_BARS) + 16;
@@ -135,6 +152,7 @@ struct MxShape {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(kWgSlots == 2 || kWgSlots == 3, "wgrad box slots");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(SFA_COL + SF_SLOTS * SF_STRIDE <= TMEM_COLS, "TMEM budget");
 };
@@ -595,7 +613,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // columns) and TMEM goes back to the MMA issuer before any byte moves
         // to the main grad: the next tile's MMAs overlap this tile's memory
         // traffic, which is what bounds the k-grouped wgrad.  Each warp then
-        // sends its rows through a ring of two 4 KB boxes (32 rows x 32 fp32,
+        // sends its rows through a ring of kWgSlots 4 KB boxes (32 rows x 32 fp32,
         // 128-byte swizzle) that lane 0 hands to the TMA unit.
         //   accumulate == 0: plain TMA stores.
         //   accumulate == 1, a tile of at least kWgRmwMinK k-tiles: the old
@@ -610,9 +628,10 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         //   repeated calls are bitwise identical.
         constexpr int WBOX = 32 * 128;
         const int q = warp & 3, h = (warp - 4) >> 2, w = warp - 4;
-        uint8_t* ring = c.out + w * 2 * WBOX;
+        constexpr int WS = kWgSlots;
+        uint8_t* ring = c.out + w * WS * WBOX;
         const uint32_t ring_addr = ptx::smem_addr(ring);
-        uint64_t* lbar = c.obar + 2 * w;                  // load barrier of each slot
+        uint64_t* lbar = c.obar + WS * w;                 // load barrier of each slot
         // box k (counted over the whole call) uses slot k & 1; per slot, bit
         // s of lph is the parity of its next load completion and bit s of
         // lpend says whether a load into it is in flight (lane 0's copy)
@@ -640,8 +659,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 // boxes 0 and 1 of this tile: both slots, once their last
                 // stores have read them
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                for (int b = 0; b < 2; ++b) {
-                    const int slot = (int)((boxes + b) & 1);
+                for (int b = 0; b < (WS < 4 ? WS : 4); ++b) {
+                    const int slot = (int)((boxes + b) % WS);
                     ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
                     ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * b, orow);
                     lpend |= 1u << slot;
@@ -673,7 +692,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             }
 #pragma unroll
             for (int b = 0; b < 4; ++b, ++boxes) {
-                const int slot = (int)(boxes & 1);
+                const int slot = (int)(boxes % WS);
                 const uint32_t box = ring_addr + slot * WBOX;
                 if (rmw) {
                     if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
@@ -692,8 +711,12 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                                                __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * j + 3]))));
                     }
                 } else {
-                    if (lane == 0)                        // the store two boxes back read this slot
-                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    if (lane == 0) {                      // the store WS boxes back read this slot
+                        if (WS == 2)
+                            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                        else
+                            asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+                    }
                     __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -708,11 +731,11 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     else
                         ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
                     ptx::bulk_commit_group();
-                    if (rmw && b + 2 < 4) {
-                        // box b + 2 into this slot once the store has read it
+                    if (rmw && b + WS < 4) {
+                        // box b + WS into this slot once the store has read it
                         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                         ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
-                        ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * (b + 2), orow);
+                        ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * (b + WS), orow);
                         lpend |= 1u << slot;
                     }
                 }
@@ -721,7 +744,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         if (lane == 0) {
             // loads still in flight (an abort) land before the CTA leaves
             volatile int no_abort = 0;
-            for (int sl = 0; sl < 2; ++sl)
+            for (int sl = 0; sl < WS; ++sl)
                 if ((lpend >> sl) & 1u)
                     ptx::mbar_wait(&lbar[sl], (lph >> sl) & 1u, &no_abort, p.status);
             ptx::bulk_wait_all();
@@ -1463,7 +1486,7 @@ gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap
         return GQ_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
     GemmArgs a = args;
-    a.front_ctas = (int)(grid / 2);
+    a.front_ctas = (int)(grid * kWgFrontPct / 100);
     kernel<<<(unsigned)grid, S::THREADS, S::SMEM, stream>>>(ma, mb, mo, a);
     return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
