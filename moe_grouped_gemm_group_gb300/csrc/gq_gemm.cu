@@ -153,6 +153,7 @@ struct MxShape {
     static constexpr int SMEM = 1024 + STAGES * STAGE + OUT_BYTES + BAR_BYTES + SCAN_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(kWgSlots == 2 || kWgSlots == 3, "wgrad box slots");
+    static_assert((SF_SLOTS & (SF_SLOTS - 1)) == 0, "scale slots: a power of two");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(SFA_COL + SF_SLOTS * SF_STRIDE <= TMEM_COLS, "TMEM budget");
 };
@@ -455,6 +456,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer --
         int64_t issued = 0, cursor = blockIdx.x, rq = 0;
+        int ps = 0;                                       // stage of the next load, its phase
+        uint32_t pph = 0;
         const bool front = (int)blockIdx.x < p.front_ctas;
         while (!*c.abort) {
             int64_t tile;
@@ -474,10 +477,13 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (t.skip || t.nk == 0)
                 continue;
             for (int kt = 0; kt < t.nk; ++kt, ++issued) {
-                const int s = (int)(issued % S::STAGES);
-                const uint32_t ph = (uint32_t)((issued / S::STAGES) & 1);
-                if (!ptx::mbar_wait(&c.empty[s], ph ^ 1u, c.abort, p.status))
+                const int s = ps;
+                if (!ptx::mbar_wait(&c.empty[s], pph ^ 1u, c.abort, p.status))
                     break;
+                if (++ps == S::STAGES) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
                 uint64_t* bar = &c.full[s];
                 ptx::mbar_arrive_expect_tx(bar, S::STAGE);
                 uint8_t* sa = c.a + s * S::A_BYTES;
@@ -546,7 +552,19 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         drain_loads(c.full, S::STAGES, issued, p.status);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------- MMA issuer --
-        int64_t consumed = 0, tiles_done = 0, cursor = blockIdx.x, rq = 0;
+        // Stage, phase and scale slot advance by one per k-tile.  Descriptors
+        // of stage 0 are built once and stepped by the stage size: their
+        // address field counts 16-byte units and stays inside its 14 bits
+        // (shared memory ends below 256 KB).
+        const uint64_t a_desc0 = A_MN ? ptx::smem_desc(ptx::smem_addr(c.a), 16384, 1024, 2)
+                                      : ptx::smem_desc(ptx::smem_addr(c.a), 16, 1024, 2);
+        const uint64_t b_desc0 = B_MN ? ptx::smem_desc(ptx::smem_addr(c.b), 16384, 1024, 2)
+                                      : ptx::smem_desc(ptx::smem_addr(c.b), 16, 1024, 2);
+        const uint64_t sfa_desc0 = ptx::smem_desc(ptx::smem_addr(c.sfa), 0, 128, 0);
+        const uint64_t sfb_desc0 = ptx::smem_desc(ptx::smem_addr(c.sfb), 0, 128, 0);
+        int s = 0;
+        uint32_t ph = 0, sf_slot = 0;
+        int64_t tiles_done = 0, cursor = blockIdx.x, rq = 0;
         while (!*c.abort) {
             int64_t tile;
             if (!dyn) {
@@ -567,36 +585,39 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::tc_fence_after_sync();
             const uint32_t d = tmem + acc * BN;
             bool ok = true;
-            for (int kt = 0; kt < t.nk; ++kt, ++consumed) {
-                const int s = (int)(consumed % S::STAGES);
-                const uint32_t ph = (uint32_t)((consumed / S::STAGES) & 1);
+            for (int kt = 0; kt < t.nk; ++kt) {
                 if (!ptx::mbar_wait(&c.full[s], ph, c.abort, p.status)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                const uint32_t sf_off = (uint32_t)(consumed % S::SF_SLOTS) * S::SF_STRIDE;
-                ptx::tc_cp_sf_atom(tmem + S::SFA_COL + sf_off,
-                                   ptx::smem_desc(ptx::smem_addr(c.sfa + s * S::SFA_BYTES), 0, 128, 0));
+                const uint32_t sfa_t = tmem + S::SFA_COL + sf_slot * S::SF_STRIDE;
+                const uint32_t sfb_t = tmem + S::SFB_COL + sf_slot * S::SF_STRIDE;
+                ptx::tc_cp_sf_atom(sfa_t, sfa_desc0 + (uint64_t)(s * (S::SFA_BYTES >> 4)));
 #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)
-                    ptx::tc_cp_sf_atom(tmem + S::SFB_COL + sf_off + 4 * j,
-                                       ptx::smem_desc(ptx::smem_addr(c.sfb + s * S::SFB_BYTES + 512 * j),
-                                                      0, 128, 0));
-                const uint32_t a_addr = ptx::smem_addr(c.a + s * S::A_BYTES);
-                const uint32_t b_addr = ptx::smem_addr(c.b + s * S::B_BYTES);
-                const int nsub = (kt == t.nk - 1) ? t.last_sub : 4;
-                for (int j = 0; j < nsub; ++j) {
+                    ptx::tc_cp_sf_atom(sfb_t + 4 * j, sfb_desc0 + (uint64_t)((s * S::SFB_BYTES + 512 * j) >> 4));
+                const uint64_t ad = a_desc0 + (uint64_t)(s * (S::A_BYTES >> 4));
+                const uint64_t bd = b_desc0 + (uint64_t)(s * (S::B_BYTES >> 4));
+                // the wgrad's last k-tile may hold fewer than 128 live rows
+                const int nsub = (KIND == GEMM_WGRAD_MX && kt == t.nk - 1) ? t.last_sub : 4;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (KIND == GEMM_WGRAD_MX && j >= nsub)
+                        break;
                     // K-major: step 32 bytes along the swizzled 128-byte row;
-                    // MN-major: step 32 rows of 128 bytes.
-                    const uint64_t ad = A_MN ? ptx::smem_desc(a_addr + 4096 * j, 16384, 1024, 2)
-                                             : ptx::smem_desc(a_addr + 32 * j, 16, 1024, 2);
-                    const uint64_t bd = B_MN ? ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2)
-                                             : ptx::smem_desc(b_addr + 32 * j, 16, 1024, 2);
-                    ptx::tc_mma_mxf8(d, ad, bd, ptx::idesc_mxf8(BM, BN, A_MN, B_MN, (uint32_t)j),
-                                     tmem + S::SFA_COL + sf_off, tmem + S::SFB_COL + sf_off, (kt | j) != 0);
+                    // MN-major: step 32 rows of 128 bytes (16-byte units).
+                    const uint64_t a_step = A_MN ? 256u * j : 2u * j;
+                    const uint64_t b_step = B_MN ? 256u * j : 2u * j;
+                    ptx::tc_mma_mxf8(d, ad + a_step, bd + b_step, ptx::idesc_mxf8(BM, BN, A_MN, B_MN, (uint32_t)j),
+                                     sfa_t, sfb_t, (kt | j) != 0);
                 }
                 ptx::tc_commit(&c.empty[s]);
+                if (++s == S::STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                sf_slot = (sf_slot + 1) & (S::SF_SLOTS - 1);
             }
             if (!ok)
                 break;
