@@ -92,7 +92,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--json-out", default=None)
     return ap.parse_args()
 
@@ -336,18 +336,74 @@ class Step:
         self.h_csplits = torch.from_numpy(self.cw.splits.copy()).pin_memory()
         self.h_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
 
+        self.s_up = torch.cuda.Stream()
+        self.s_down = torch.cuda.Stream()
+        self.ev_used = {}       # input -> its last use in the previous step
+        self.ev_read = {}       # output -> its copy to the host in the previous step
+
+    # Which buffers each launch reads from the host's inputs and which of the
+    # copied-back results it writes.
+    E2E_INPUTS = {"quant_x1": ("x1",), "quant_w1": ("w1",), "quant_x2": ("x2",), "quant_w2": ("w2",),
+                  "quant_dy2": ("dy2",), "quant_dy1": ("dy1",), "quant_ch_dy": ("c_dy",), "quant_ch_x": ("c_x",)}
+    E2E_OUTPUTS = {"fprop1": ("y1",), "fprop2": ("y2",), "dgrad2": ("dx2",), "wgrad2": ("dw2",),
+                   "dgrad1": ("dx1",), "wgrad1": ("dw1",), "wgrad_ch": ("cdw",)}
+
+    def _e2e_dev(self, k):
+        return self.cin[k[2:]] if k.startswith("c_") else self.inputs[k]
+
+    def _e2e_host(self, k):
+        return self.h_cin[k[2:]] if k.startswith("c_") else self.h_in[k]
+
     def run_e2e(self):
-        for k, v in self.h_in.items():
-            self.inputs[k].copy_(v, non_blocking=True)
-        for k, v in self.h_cin.items():
-            self.cin[k].copy_(v, non_blocking=True)
+        """One step with its inputs uploaded from pinned host memory and every
+        result downloaded, all copies on their own streams: an input is
+        uploaded once the previous step's last reader of its buffer is done,
+        a result is downloaded as soon as its launch is, and a launch that
+        rewrites a result waits for the previous step's download of it."""
+        torch = self.torch
+        cur = torch.cuda.current_stream()
         self.splits.copy_(self.h_splits, non_blocking=True)
         self.csplits.copy_(self.h_csplits, non_blocking=True)
-        self.run()
-        for k, v in self.out.items():
-            self.h_out[k].copy_(v, non_blocking=True)
-        self.h_cdw.copy_(self.cdw, non_blocking=True)
-        self.h_status.copy_(self.status, non_blocking=True)
+        ready = {}
+        with torch.cuda.stream(self.s_up):
+            for name, _, _, _ in self.launches:
+                for k in self.E2E_INPUTS.get(name, ()):
+                    if k in self.ev_used:
+                        self.s_up.wait_event(self.ev_used[k])
+                    self._e2e_dev(k).copy_(self._e2e_host(k), non_blocking=True)
+                    ready[k] = torch.cuda.Event()
+                    ready[k].record(self.s_up)
+        produced = []
+        for name, _, fn, _ in self.launches:
+            for k in self.E2E_INPUTS.get(name, ()):
+                cur.wait_event(ready[k])
+            for o in self.E2E_OUTPUTS.get(name, ()):
+                if o in self.ev_read:
+                    cur.wait_event(self.ev_read[o])
+            fn()
+            done = torch.cuda.Event()
+            done.record(cur)
+            for k in self.E2E_INPUTS.get(name, ()):
+                self.ev_used[k] = done
+            for o in self.E2E_OUTPUTS.get(name, ()):
+                produced.append((o, done))
+        last = torch.cuda.Event()
+        last.record(cur)
+        with torch.cuda.stream(self.s_down):
+            for o, ev in produced:
+                self.s_down.wait_event(ev)
+                src, dst = (self.cdw, self.h_cdw) if o == "cdw" else (self.out[o], self.h_out[o])
+                dst.copy_(src, non_blocking=True)
+                self.ev_read[o] = torch.cuda.Event()
+                self.ev_read[o].record(self.s_down)
+            self.s_down.wait_event(last)
+            self.h_status.copy_(self.status, non_blocking=True)
+
+    def e2e_join(self):
+        """Make the current stream wait for every copy issued so far."""
+        cur = self.torch.cuda.current_stream()
+        cur.wait_stream(self.s_up)
+        cur.wait_stream(self.s_down)
 
 
 def summarize(step, events, peaks, peak_kind):
@@ -501,8 +557,11 @@ def main():
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
+        step.s_up.wait_stream(torch.cuda.current_stream())
+        step.s_down.wait_stream(torch.cuda.current_stream())
         for _ in range(args.e2e_steps):
             step.run_e2e()
+        step.e2e_join()
         b.record()
         torch.cuda.synchronize()
         dist.barrier()

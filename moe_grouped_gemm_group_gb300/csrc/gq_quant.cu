@@ -57,6 +57,19 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b)
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
+// Four codes (x0's in the low byte) of (x0, x1, x2, x3) scaled by (s0, s1,
+// s2, s3): two packed fp32x2 multiplies (round to nearest, subnormals kept;
+// the products are exact, powers of two times bf16 values) and two
+// conversions.
+__device__ __forceinline__ uint32_t scale_cvt4(float x0, float x1, float x2, float x3, float s0, float s1,
+                                               float s2, float s3)
+{
+    const float2 lo = __fmul2_rn(make_float2(x0, x1), make_float2(s0, s1));
+    const float2 hi = __fmul2_rn(make_float2(x2, x3), make_float2(s2, s3));
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3) |
+           ((uint32_t)__nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3) << 16);
+}
+
 __device__ __forceinline__ void load_row32(const uint16_t* __restrict__ p, uint32_t (&v)[16])
 {
     const uint4* q = reinterpret_cast<const uint4*>(p);
@@ -277,8 +290,7 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
                 uint32_t w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    w[i] = cvt_e4m3x2(xf[4 * i] * sc, xf[4 * i + 1] * sc) |
-                           (cvt_e4m3x2(xf[4 * i + 2] * sc, xf[4 * i + 3] * sc) << 16);
+                    w[i] = scale_cvt4(xf[4 * i], xf[4 * i + 1], xf[4 * i + 2], xf[4 * i + 3], sc, sc, sc, sc);
                 // 32 codes = 16-byte chunks 2 cb and 2 cb + 1 of the row
                 ptx::sts128(rd_box + ptx::swz128(r_in_tile, 2 * cb), make_uint4(w[0], w[1], w[2], w[3]));
                 ptx::sts128(rd_box + ptx::swz128(r_in_tile, 2 * cb + 1), make_uint4(w[4], w[5], w[6], w[7]));
@@ -331,8 +343,8 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
                 uint32_t w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    w[i] = cvt_e4m3x2(xf[4 * i] * sc[4 * i], xf[4 * i + 1] * sc[4 * i + 1]) |
-                           (cvt_e4m3x2(xf[4 * i + 2] * sc[4 * i + 2], xf[4 * i + 3] * sc[4 * i + 3]) << 16);
+                    w[i] = scale_cvt4(xf[4 * i], xf[4 * i + 1], xf[4 * i + 2], xf[4 * i + 3], sc[4 * i],
+                                      sc[4 * i + 1], sc[4 * i + 2], sc[4 * i + 3]);
                 ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb), make_uint4(w[0], w[1], w[2], w[3]));
                 ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb + 1), make_uint4(w[4], w[5], w[6], w[7]));
             }
