@@ -93,6 +93,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay measurement of the step")
     ap.add_argument("--json-out", default=None)
     return ap.parse_args()
 
@@ -547,6 +549,32 @@ def main():
     qms = sum(rows[n]["ms"] for n, k, _, _ in step.launches if k == "q")
     gms = sum(rows[n]["ms"] for n, k, _, _ in step.launches if k == "g")
 
+    # the same step captured once in a CUDA graph and replayed (launch
+    # overhead out of the picture; split sizes stay on the device)
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step.run()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        dist.barrier()
+        g_ms = dist.max(a.elapsed_time(b)) / args.steps
+        if int(step.status.item()) != 0:
+            raise SystemExit("device status set in the graph region")
+        graph = {"value": round(job_value(step.gemm_flops, dist.world, g_ms) / 1e12, 2), "unit": "TFLOP/s",
+                 "ms_per_step": round(g_ms, 4), "launches_per_step": len(step.launches)}
+        del g
+
     e2e = None
     if not args.no_e2e:
         step.setup_e2e()
@@ -590,7 +618,7 @@ def main():
         "quantize_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(qbytes / (qms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4),
         "gemm_tflops": round(step.gemm_flops / (gms * 1e-3) / 1e12, 1),
-        "roofline": roof, "breakdown": rows, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roof, "breakdown": rows, "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
         "gpu_launches": len(step.launches) * args.steps, "clocks": clk,
     }
     if dist.rank == 0:

@@ -1494,7 +1494,7 @@ __global__ void k_zero_fill(float* __restrict__ out, int64_t count, const int32_
 template <typename Kernel>
 cudaError_t prepare(Kernel kernel, int smem)
 {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return prepare_kernel(reinterpret_cast<const void*>(kernel), smem, 0, nullptr);
 }
 
 template <int KIND, int BN, bool OUT_BF16>

@@ -32,6 +32,48 @@ const DeviceInfo& device_info()
     return infos[dev];
 }
 
+cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* blocks_per_sm)
+{
+    struct Entry {
+        const void* fn;
+        int dev, dyn_smem, threads, per_sm;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        const Entry& e = cache[i];
+        if (e.fn == fn && e.dev == dev && e.dyn_smem == dyn_smem && e.threads == threads) {
+            if (blocks_per_sm)
+                *blocks_per_sm = e.per_sm;
+            return cudaSuccess;
+        }
+    }
+    if (dyn_smem > 48 * 1024) {
+        const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+        if (err != cudaSuccess)
+            return err;
+    }
+    int n = 1;
+    if (threads > 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, (size_t)dyn_smem) != cudaSuccess) {
+            (void)cudaGetLastError();            // leave no error behind for the launch check
+            n = 1;
+        }
+        if (n < 1)
+            n = 1;
+    }
+    if (used < 256)
+        cache[used++] = Entry{fn, dev, dyn_smem, threads, n};
+    if (blocks_per_sm)
+        *blocks_per_sm = n;
+    return cudaSuccess;
+}
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()

@@ -20,6 +20,11 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();
 
+// Per (kernel, device) set-up, done on the first launch there and cached:
+// the dynamic shared-memory limit and the resident blocks per SM.  Later
+// launches only enqueue work.
+cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* blocks_per_sm);
+
 // 2-D tensor map over a row-major [rows, cols] buffer of `elem_bytes`-byte
 // elements (rows stride = cols * elem_bytes), boxes of box_cols x box_rows
 // with the 128-byte swizzle; out-of-range elements read as zero.  False if

@@ -458,8 +458,8 @@ k_quant_ch(const uint16_t* __restrict__ x, int64_t rows_cap, int64_t cols,
 
 int blocks_per_sm_for(const void* fn, int threads)
 {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1)
+    int n = 1;
+    if (prepare_kernel(fn, 0, threads, &n) != cudaSuccess)
         n = 1;
     return n;
 }
@@ -492,13 +492,10 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const
     const int64_t tiles_bound = ((rows_cap + 127) / 128 + G) * (cols / 128);
     const int sms = device_info().sm_count;
     auto go = [&](auto kernel) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+        int per_sm = 1;
+        const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kernel), kQSmem, kQThreadsMx, &per_sm);
         if (e != cudaSuccess)
             return e;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQThreadsMx, kQSmem) != cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, tiles_bound));
         kernel<<<(unsigned)grid, kQThreadsMx, kQSmem, stream>>>(map, om, rows_cap, cols, splits, G, row_scale,
                                                                 col_scale, status);

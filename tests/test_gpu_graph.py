@@ -1,0 +1,102 @@
+"""CUDA-graph capture of a whole grouped-linear step: fc1 and fc2 forward,
+dgrad and wgrad (accumulating into fp32 main grads), every quantisation
+included, with the split sizes on the device.  The step is captured once and
+replayed with new split sizes and new inputs written into the same buffers;
+each replay must give, bit for bit, what eager calls give on the same
+inputs (TransformerEngine PR 3224: device split sizes, no host sync)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import moe_grouped_gemm_group_gb300 as gq  # noqa: E402
+from _gpu_util import DEV, check_status  # noqa: E402
+
+G, H, F, R = 4, 512, 256, 1024
+SPLITS = [np.array([256, 0, 416, 288], np.int32), np.array([96, 512, 32, 320], np.int32)]
+
+
+class Layer:
+    def __init__(self):
+        mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+        self.mx = mx
+        bf = torch.bfloat16
+        self.inp = {"x1": torch.empty((R, H), dtype=bf, device=DEV), "x2": torch.empty((R, F), dtype=bf, device=DEV),
+                    "dy1": torch.empty((R, F), dtype=bf, device=DEV), "dy2": torch.empty((R, H), dtype=bf, device=DEV),
+                    "w1": torch.empty((G * F, H), dtype=bf, device=DEV),
+                    "w2": torch.empty((G * H, F), dtype=bf, device=DEV)}
+        shape = {"x1": (R, H), "x2": (R, F), "dy1": (R, F), "dy2": (R, H), "w1": (G * F, H), "w2": (G * H, F)}
+        self.q = {k: gq.alloc_quantized(r, c, G, mx, DEV) for k, (r, c) in shape.items()}
+        self.out = {"y1": torch.empty((R, F), dtype=bf, device=DEV), "y2": torch.empty((R, H), dtype=bf, device=DEV),
+                    "dx2": torch.empty((R, F), dtype=bf, device=DEV), "dx1": torch.empty((R, H), dtype=bf, device=DEV),
+                    "dw1": torch.empty((G, F, H), device=DEV), "dw2": torch.empty((G, H, F), device=DEV)}
+        self.splits = torch.zeros(G, dtype=torch.int32, device=DEV)
+        self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        self.ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=DEV)
+
+    def load(self, seed, splits):
+        gen = torch.Generator(device=DEV).manual_seed(seed)
+        for k, t in self.inp.items():
+            t.copy_(torch.randn(t.shape, generator=gen, device=DEV) * (0.02 if k.startswith("w") else 1.0))
+        for k in ("dw1", "dw2"):
+            self.out[k].copy_(torch.randn(self.out[k].shape, generator=gen, device=DEV) * 1e-3)
+        for k in ("y1", "y2", "dx1", "dx2"):
+            self.out[k].fill_(float("nan"))
+        self.splits.copy_(torch.from_numpy(splits))
+
+    def step(self):
+        i, q, o, sp, st, mx = self.inp, self.q, self.out, self.splits, self.status, self.mx
+        bf16 = gq.DTYPE_BF16
+        gq.gq_quantize(i["x1"], sp, G, mx, q["x1"], st)
+        gq.gq_quantize(i["w1"], None, G, mx, q["w1"], st)
+        gq.gq_gemm_fprop(q["x1"], q["w1"], sp, G, F, H, o["y1"], bf16, st)
+        gq.gq_quantize(i["x2"], sp, G, mx, q["x2"], st)
+        gq.gq_quantize(i["w2"], None, G, mx, q["w2"], st)
+        gq.gq_gemm_fprop(q["x2"], q["w2"], sp, G, H, F, o["y2"], bf16, st)
+        gq.gq_quantize(i["dy2"], sp, G, mx, q["dy2"], st)
+        gq.gq_gemm_dgrad(q["dy2"], q["w2"], sp, G, H, F, o["dx2"], bf16, st)
+        gq.gq_gemm_wgrad(q["dy2"], q["x2"], sp, G, H, F, o["dw2"], True, st, workspace=self.ws)
+        gq.gq_quantize(i["dy1"], sp, G, mx, q["dy1"], st)
+        gq.gq_gemm_dgrad(q["dy1"], q["w1"], sp, G, F, H, o["dx1"], bf16, st)
+        gq.gq_gemm_wgrad(q["dy1"], q["x1"], sp, G, F, H, o["dw1"], True, st, workspace=self.ws)
+
+    def results(self):
+        torch.cuda.synchronize()
+        check_status(self.status)
+        return {k: v.clone() for k, v in self.out.items()}
+
+
+def _same_bits(a, b):
+    ia = a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32)
+    ib = b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)
+    return torch.equal(ia, ib)
+
+
+def test_captured_step_replays_like_eager_calls():
+    layer = Layer()
+    layer.load(0, SPLITS[0])
+    layer.step()                          # first calls on the device: set-up outside capture
+    layer.results()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.step()
+
+    for trial, splits in enumerate(SPLITS):
+        layer.load(10 + trial, splits)
+        graph.replay()
+        got = layer.results()
+        layer.load(10 + trial, splits)
+        layer.step()
+        want = layer.results()
+        L = int(splits.sum())
+        for k in want:
+            g, w = (got[k][:L], want[k][:L]) if k in ("y1", "y2", "dx1", "dx2") else (got[k], want[k])
+            assert _same_bits(g, w), f"replay {trial}: {k} differs from the eager result"
+        # the live rows were written; the rows past the live total were not
+        assert not torch.isnan(got["y1"][:L].float()).any()
+        assert torch.isnan(got["y1"][L:].float()).all()
