@@ -74,9 +74,14 @@ def _load():
                                            [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_int64,
                                             C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
                                             C.c_void_p])
+            lib.or_grouped_bias_add.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int64,
+                                                C.c_int64]
+            lib.or_grouped_bias_grad.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, C.c_int64,
+                                                 C.c_void_p]
             for name in ("or_split_scan", "or_quantize_mx", "or_quantize_channel",
                          "or_gemm_fprop", "or_gemm_dgrad", "or_gemm_wgrad_mx",
-                         "or_gemm_wgrad_channel", "or_gemm_sample"):
+                         "or_gemm_wgrad_channel", "or_gemm_sample", "or_grouped_bias_add",
+                         "or_grouped_bias_grad"):
                 getattr(lib, name).restype = C.c_int
             _lib = lib
     return _lib
@@ -225,6 +230,30 @@ def gemm_fprop(xq: MXQuantized, wq: MXQuantized, splits, num_groups, N, K,
                            _p(wq.row_scale), _p(_splits(splits)), num_groups, R, N, K, _p(y))
     _check(st, "gemm_fprop")
     return y
+
+
+def grouped_bias_add(y: np.ndarray, bias: np.ndarray, splits, num_groups) -> np.ndarray:
+    """y[o_g + r, :] += bias[g] for the live rows of every group, in place on
+    a C-contiguous fp64 [R, N] array; returns y."""
+    lib = _load()
+    assert y.dtype == np.float64 and y.flags.c_contiguous
+    R, N = y.shape
+    b = np.ascontiguousarray(bias, np.float64).reshape(num_groups, N)
+    st = lib.or_grouped_bias_add(_p(y), _p(b), _p(_splits(splits)), num_groups, R, N)
+    _check(st, "grouped_bias_add")
+    return y
+
+
+def grouped_bias_grad(dy_bits: np.ndarray, splits, num_groups) -> np.ndarray:
+    """Per-group column sums of the live rows of a bf16 [R, C] buffer (given
+    as uint16 bits), fp64 [G, C]."""
+    lib = _load()
+    dy = np.ascontiguousarray(dy_bits, np.uint16)
+    R, Cc = dy.shape
+    db = np.empty((num_groups, Cc))
+    st = lib.or_grouped_bias_grad(_p(dy), _p(_splits(splits)), num_groups, R, Cc, _p(db))
+    _check(st, "grouped_bias_grad")
+    return db
 
 
 def gemm_dgrad(dyq: MXQuantized, wq: MXQuantized, splits, num_groups, N, K,

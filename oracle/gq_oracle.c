@@ -22,6 +22,10 @@
  *    dequantised operands, accumulated in fp64 (TransformerEngine issue 3484,
  *    "Additional context: Scope"; DeepGEMM issue 365, the fp32 reference
  *    ref[e] = gy_e.t() @ s_e with empty experts skipped).
+ *  - Grouped bias add y += b_g over each group's live rows, and the bias
+ *    gradient db_g = column sums of dY over the group's live rows
+ *    (TransformerEngine PR 3224: launch_grouped_bias_add with its zero-row
+ *    guard, and the dbiases of the backward).
  *
  * Readings taken where the pages are silent (each listed in the design notes):
  *  - FP8 is float8_e4m3fn: bias 7, max 448, no infinities, NaN = S.1111.111,
@@ -635,5 +639,55 @@ int or_gemm_sample(int kind, const uint8_t* a_data, const void* a_scale, const u
     }
     free(sa.buf);
     free(sb.buf);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped bias add and bias gradient                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Bias add: y[o_g + r, n] += bias[g, n] for every live row r of group g --
+ * the grouped bias add that follows the grouped GEMM in TransformerEngine
+ * PR 3224's forward sequence (launch_grouped_bias_add), which returns
+ * before touching any data when the token total is 0.  Rows past the live
+ * total are not touched.  MX split alignment (multiples of 32). */
+int or_grouped_bias_add(double* y, const double* bias, const int32_t* splits, int G, int64_t rows_cap,
+                        int64_t N)
+{
+    int64_t off[1025], tp[1025], sb[1025];
+    if (G < 1 || G > 1024 || N <= 0)
+        return OR_ERR_INVALID_ARG;
+    int st = or_split_scan(splits, G, rows_cap, N, OR_RECIPE_MX, off, tp, sb);
+    if (st != OR_OK)
+        return st;
+    if (off[G] == 0)
+        return OR_OK;
+    for (int g = 0; g < G; ++g)
+        for (int64_t r = off[g]; r < off[g + 1]; ++r)
+            for (int64_t n = 0; n < N; ++n)
+                y[r * N + n] += bias[(int64_t)g * N + n];
+    return OR_OK;
+}
+
+/* Bias gradient: db[g, c] = sum of dy[r, c] over the live rows r of group g,
+ * in fp64 on the bf16 values -- the per-group dbiases that the grouped
+ * linear's backward returns beside dinput and dweights (TransformerEngine
+ * PR 3224, sequence diagram).  An empty group gets 0. */
+int or_grouped_bias_grad(const uint16_t* dy, const int32_t* splits, int G, int64_t rows_cap, int64_t C,
+                         double* db)
+{
+    int64_t off[1025], tp[1025], sb[1025];
+    if (G < 1 || G > 1024 || C <= 0)
+        return OR_ERR_INVALID_ARG;
+    int st = or_split_scan(splits, G, rows_cap, C, OR_RECIPE_MX, off, tp, sb);
+    if (st != OR_OK)
+        return st;
+    for (int g = 0; g < G; ++g)
+        for (int64_t c = 0; c < C; ++c) {
+            double acc = 0.0;
+            for (int64_t r = off[g]; r < off[g + 1]; ++r)
+                acc += bf16_value(dy[r * C + c]);
+            db[(int64_t)g * C + c] = acc;
+        }
     return OR_OK;
 }
