@@ -171,6 +171,30 @@ gq_status gq_quantize(const void* x_bf16, int64_t rows_cap, int64_t cols,
                       gq_quantized* out, int32_t* d_status, gq_stream_t stream);
 
 /*
+ * gq_quantize_dbias -- gq_quantize (MX recipe) of an output gradient dY
+ * fused with its bias gradient, the per-group dbiases that the grouped
+ * linear's backward returns beside dinput and dweights (TransformerEngine
+ * PR 3224, sequence diagram):
+ *   d_dbias[g, c] = sum of dY[r, c] over the live rows r of group g
+ * The quantiser sums each 128 x 128 tile's columns while it has them in
+ * registers (one fp32 sum per column, in a fixed order) and writes them to
+ * d_workspace; a second small kernel adds each group's tile sums in tile
+ * order, so the result is the same on every call.
+ *   d_dbias     : fp32 [num_groups, cols], 16-byte aligned; empty groups
+ *                 (and L == 0) get 0.
+ *   d_workspace : caller-owned device memory of at least
+ *                 gq_dbias_workspace_bytes(num_groups, rows_cap, cols) bytes,
+ *                 16-byte aligned; its content on entry does not matter.
+ * Everything else as gq_quantize; GQ_ERR_UNSUPPORTED for the per-channel
+ * recipe.
+ */
+uint64_t gq_dbias_workspace_bytes(int32_t num_groups, int64_t rows_cap, int64_t cols);
+gq_status gq_quantize_dbias(const void* x_bf16, int64_t rows_cap, int64_t cols,
+                            const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
+                            gq_quantized* out, float* d_dbias, void* d_workspace, uint64_t workspace_bytes,
+                            int32_t* d_status, gq_stream_t stream);
+
+/*
  * gq_gemm_fprop -- Y_g = X_g W_g^T for every group g (TransformerEngine PR
  * 3224, general_grouped_gemm_for_grouped_tensor in the forward sequence).
  *   x : MX rowwise, rows_cap R, cols k, split by d_split_sizes.
@@ -183,6 +207,23 @@ gq_status gq_quantize(const void* x_bf16, int64_t rows_cap, int64_t cols,
 gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
                         const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
                         void* y, int32_t out_dtype, int32_t* d_status, gq_stream_t stream);
+
+/*
+ * gq_gemm_fprop_bias -- Y_g = X_g W_g^T + b_g: gq_gemm_fprop with the
+ * grouped bias add that TransformerEngine PR 3224 runs after the grouped
+ * GEMM (launch_grouped_bias_add in its forward sequence diagram), fused into
+ * the GEMM's epilogue: the bias is added to the fp32 accumulator before the
+ * conversion to out_dtype, so Y is written once.
+ *   d_bias : [num_groups, n] device array of bias_dtype (GQ_DTYPE_F32 or
+ *            GQ_DTYPE_BF16), 16-byte aligned; row g is added to every live
+ *            row of group g.  Empty groups and L == 0 touch nothing (the
+ *            page's zero-row guard).
+ * Everything else as gq_gemm_fprop.
+ */
+gq_status gq_gemm_fprop_bias(const gq_quantized* x, const gq_quantized* w,
+                             const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                             const void* d_bias, int32_t bias_dtype, void* y, int32_t out_dtype,
+                             int32_t* d_status, gq_stream_t stream);
 
 /*
  * gq_gemm_dgrad -- dX_g = dY_g W_g (TransformerEngine issue 3484: M is a

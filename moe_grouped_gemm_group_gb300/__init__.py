@@ -17,6 +17,7 @@ __all__ = [
     "GQError", "Recipe", "Quantized", "GroupedTensor", "load", "library_path",
     "gq_status_string", "gq_version", "gq_scale_bytes_bound", "gq_split_scan", "gq_quantize",
     "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_gemm_wgrad_noalloc", "alloc_quantized",
+    "gq_gemm_fprop_bias", "gq_quantize_dbias", "gq_dbias_workspace_bytes",
     "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "DTYPE_F32", "DTYPE_BF16", "STATUS",
 ]
 
@@ -86,6 +87,13 @@ def load():
             f.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         lib.gq_gemm_wgrad.restype = i32
         lib.gq_gemm_wgrad.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, C.c_uint64, vp, vp]
+        lib.gq_gemm_fprop_bias.restype = i32
+        lib.gq_gemm_fprop_bias.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, i32, vp, vp]
+        lib.gq_dbias_workspace_bytes.restype = C.c_uint64
+        lib.gq_dbias_workspace_bytes.argtypes = [i32, i64, i64]
+        lib.gq_quantize_dbias.restype = i32
+        lib.gq_quantize_dbias.argtypes = [vp, i64, i64, vp, i32, C.POINTER(Recipe), qp, vp, vp, C.c_uint64,
+                                          vp, vp]
         lib.gq_gemm_wgrad_noalloc.restype = i32
         lib.gq_gemm_wgrad_noalloc.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         _lib = lib
@@ -225,6 +233,38 @@ def gq_gemm_fprop(x: GroupedTensor, w: GroupedTensor, splits, num_groups: int, n
                               num_groups, n, k, _ptr(y, "y"), out_dtype, _ptr(status, "status"),
                               _stream(stream))
     _check(st, "gq_gemm_fprop")
+
+
+def gq_gemm_fprop_bias(x: GroupedTensor, w: GroupedTensor, splits, num_groups: int, n: int, k: int, bias,
+                       y, out_dtype: int, status, stream=None) -> None:
+    """gq_gemm_fprop plus the per-group bias ``bias`` ([num_groups, n], fp32
+    or bf16 CUDA tensor) added in the GEMM's epilogue."""
+    import torch
+    bias_dtype = DTYPE_BF16 if bias.dtype == torch.bfloat16 else DTYPE_F32
+    if bias.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"bias must be fp32 or bf16, got {bias.dtype}")
+    st = load().gq_gemm_fprop_bias(C.byref(x.desc), C.byref(w.desc), _ptr(splits, "splits", False),
+                                   num_groups, n, k, _ptr(bias, "bias"), bias_dtype, _ptr(y, "y"), out_dtype,
+                                   _ptr(status, "status"), _stream(stream))
+    _check(st, "gq_gemm_fprop_bias")
+
+
+def gq_dbias_workspace_bytes(num_groups: int, rows_cap: int, cols: int) -> int:
+    return int(load().gq_dbias_workspace_bytes(num_groups, rows_cap, cols))
+
+
+def gq_quantize_dbias(x, splits, num_groups: int, recipe: Recipe, out: GroupedTensor, dbias, workspace,
+                      status, stream=None) -> None:
+    """gq_quantize (MX) of a gradient ``x`` fused with its per-group column
+    sums into ``dbias`` (fp32 [num_groups, cols]); ``workspace`` is a CUDA
+    tensor of at least gq_dbias_workspace_bytes(...) bytes."""
+    rows_cap, cols = (int(x.shape[0]), int(x.shape[1])) if x is not None else (0, out.cols)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().gq_quantize_dbias(_ptr(x, "x", rows_cap > 0), rows_cap, cols, _ptr(splits, "splits", False),
+                                  num_groups, C.byref(recipe), C.byref(out.desc), _ptr(dbias, "dbias"),
+                                  _ptr(workspace, "workspace"), ws_bytes, _ptr(status, "status"),
+                                  _stream(stream))
+    _check(st, "gq_quantize_dbias")
 
 
 def gq_gemm_dgrad(dy: GroupedTensor, w: GroupedTensor, splits, num_groups: int, n: int, k: int,

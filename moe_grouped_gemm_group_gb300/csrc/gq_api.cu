@@ -43,6 +43,74 @@ gq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GQ_OK : GQ_ERR_
 
 }  // namespace
 
+namespace {
+
+gq_status quantize_impl(const void* x_bf16, int64_t rows_cap, int64_t cols,
+                        const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
+                        gq_quantized* out, int32_t* d_status, gq_stream_t stream, float* dpart)
+{
+    if (!recipe || !out || !d_status)
+        return GQ_ERR_INVALID_ARG;
+    gq_status st = check_partition(d_split_sizes, num_groups, rows_cap, cols);
+    if (st != GQ_OK)
+        return st;
+    if (out->num_groups != num_groups || out->rows_cap != rows_cap || out->cols != cols ||
+        out->recipe.kind != recipe->kind)
+        return GQ_ERR_SHAPE_MISMATCH;
+    const bool live = rows_cap > 0;
+    if (live && (!x_bf16 || !aligned16(x_bf16)))
+        return x_bf16 ? GQ_ERR_ALIGNMENT : GQ_ERR_INVALID_ARG;
+
+    if (recipe->kind == GQ_RECIPE_MXFP8_1X32) {
+        if (!recipe->rowwise && !recipe->colwise)
+            return GQ_ERR_INVALID_ARG;
+        const uint64_t need = mx_scale_bound(num_groups, rows_cap, cols);
+        if (recipe->rowwise) {
+            if (live && (!out->row_data || !out->row_scale))
+                return GQ_ERR_INVALID_ARG;
+            if (live && (!aligned16(out->row_data) || !aligned16(out->row_scale)))
+                return GQ_ERR_ALIGNMENT;
+            if (out->row_scale_bytes < need)
+                return GQ_ERR_INVALID_ARG;
+        }
+        if (recipe->colwise) {
+            if (live && (!out->col_data || !out->col_scale))
+                return GQ_ERR_INVALID_ARG;
+            if (live && (!aligned16(out->col_data) || !aligned16(out->col_scale)))
+                return GQ_ERR_ALIGNMENT;
+            if (out->col_scale_bytes < need)
+                return GQ_ERR_INVALID_ARG;
+        }
+        out->recipe = *recipe;
+        if (!live)
+            return GQ_OK;
+        return cuda_status(gq::launch_quant_mx(
+            x_bf16, rows_cap, cols, d_split_sizes, num_groups,
+            recipe->rowwise ? (uint8_t*)out->row_data : nullptr, (uint8_t*)out->row_scale,
+            recipe->colwise ? (uint8_t*)out->col_data : nullptr, (uint8_t*)out->col_scale,
+            d_status, (cudaStream_t)stream, dpart));
+    }
+    if (recipe->kind == GQ_RECIPE_CHANNEL128_F32) {
+        if (recipe->rowwise || !recipe->colwise)
+            return GQ_ERR_UNSUPPORTED;
+        if (live && (!out->col_data || !out->col_scale))
+            return GQ_ERR_INVALID_ARG;
+        if (live && (!aligned16(out->col_data) || !aligned16(out->col_scale)))
+            return GQ_ERR_ALIGNMENT;
+        if (out->col_scale_bytes < channel_scale_bound(rows_cap, cols))
+            return GQ_ERR_INVALID_ARG;
+        out->recipe = *recipe;
+        if (!live)
+            return GQ_OK;
+        return cuda_status(gq::launch_quant_channel(
+            x_bf16, rows_cap, cols, d_split_sizes, num_groups, recipe->zero_scale,
+            (uint8_t*)out->col_data, (float*)out->col_scale, d_status, (cudaStream_t)stream));
+    }
+    return GQ_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* gq_status_string(int32_t status)
@@ -95,64 +163,38 @@ gq_status gq_quantize(const void* x_bf16, int64_t rows_cap, int64_t cols,
                       const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
                       gq_quantized* out, int32_t* d_status, gq_stream_t stream)
 {
-    if (!recipe || !out || !d_status)
+    return quantize_impl(x_bf16, rows_cap, cols, d_split_sizes, num_groups, recipe, out, d_status, stream,
+                         nullptr);
+}
+
+uint64_t gq_dbias_workspace_bytes(int32_t num_groups, int64_t rows_cap, int64_t cols)
+{
+    if (num_groups < 1 || rows_cap < 0 || cols <= 0 || cols % 128 != 0)
+        return 0;
+    return 4ull * (uint64_t)cols * (uint64_t)((rows_cap + 127) / 128 + num_groups);
+}
+
+gq_status gq_quantize_dbias(const void* x_bf16, int64_t rows_cap, int64_t cols,
+                            const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
+                            gq_quantized* out, float* d_dbias, void* d_workspace, uint64_t workspace_bytes,
+                            int32_t* d_status, gq_stream_t stream)
+{
+    if (!recipe || !d_dbias || !d_workspace)
         return GQ_ERR_INVALID_ARG;
-    gq_status st = check_partition(d_split_sizes, num_groups, rows_cap, cols);
+    if (recipe->kind != GQ_RECIPE_MXFP8_1X32)
+        return GQ_ERR_UNSUPPORTED;
+    if (!aligned16(d_dbias) || !aligned16(d_workspace))
+        return GQ_ERR_ALIGNMENT;
+    if (workspace_bytes < gq_dbias_workspace_bytes(num_groups, rows_cap, cols))
+        return GQ_ERR_INVALID_ARG;
+    gq_status st = quantize_impl(x_bf16, rows_cap, cols, d_split_sizes, num_groups, recipe, out, d_status,
+                                 stream, static_cast<float*>(d_workspace));
     if (st != GQ_OK)
         return st;
-    if (out->num_groups != num_groups || out->rows_cap != rows_cap || out->cols != cols ||
-        out->recipe.kind != recipe->kind)
-        return GQ_ERR_SHAPE_MISMATCH;
-    const bool live = rows_cap > 0;
-    if (live && (!x_bf16 || !aligned16(x_bf16)))
-        return x_bf16 ? GQ_ERR_ALIGNMENT : GQ_ERR_INVALID_ARG;
-
-    if (recipe->kind == GQ_RECIPE_MXFP8_1X32) {
-        if (!recipe->rowwise && !recipe->colwise)
-            return GQ_ERR_INVALID_ARG;
-        const uint64_t need = mx_scale_bound(num_groups, rows_cap, cols);
-        if (recipe->rowwise) {
-            if (live && (!out->row_data || !out->row_scale))
-                return GQ_ERR_INVALID_ARG;
-            if (live && (!aligned16(out->row_data) || !aligned16(out->row_scale)))
-                return GQ_ERR_ALIGNMENT;
-            if (out->row_scale_bytes < need)
-                return GQ_ERR_INVALID_ARG;
-        }
-        if (recipe->colwise) {
-            if (live && (!out->col_data || !out->col_scale))
-                return GQ_ERR_INVALID_ARG;
-            if (live && (!aligned16(out->col_data) || !aligned16(out->col_scale)))
-                return GQ_ERR_ALIGNMENT;
-            if (out->col_scale_bytes < need)
-                return GQ_ERR_INVALID_ARG;
-        }
-        out->recipe = *recipe;
-        if (!live)
-            return GQ_OK;
-        return cuda_status(gq::launch_quant_mx(
-            x_bf16, rows_cap, cols, d_split_sizes, num_groups,
-            recipe->rowwise ? (uint8_t*)out->row_data : nullptr, (uint8_t*)out->row_scale,
-            recipe->colwise ? (uint8_t*)out->col_data : nullptr, (uint8_t*)out->col_scale,
-            d_status, (cudaStream_t)stream));
-    }
-    if (recipe->kind == GQ_RECIPE_CHANNEL128_F32) {
-        if (recipe->rowwise || !recipe->colwise)
-            return GQ_ERR_UNSUPPORTED;
-        if (live && (!out->col_data || !out->col_scale))
-            return GQ_ERR_INVALID_ARG;
-        if (live && (!aligned16(out->col_data) || !aligned16(out->col_scale)))
-            return GQ_ERR_ALIGNMENT;
-        if (out->col_scale_bytes < channel_scale_bound(rows_cap, cols))
-            return GQ_ERR_INVALID_ARG;
-        out->recipe = *recipe;
-        if (!live)
-            return GQ_OK;
-        return cuda_status(gq::launch_quant_channel(
-            x_bf16, rows_cap, cols, d_split_sizes, num_groups, recipe->zero_scale,
-            (uint8_t*)out->col_data, (float*)out->col_scale, d_status, (cudaStream_t)stream));
-    }
-    return GQ_ERR_UNSUPPORTED;
+    // with L == 0 (rows_cap == 0 included) every group sums no tile: zeros
+    return cuda_status(gq::launch_dbias_reduce(d_split_sizes, num_groups, rows_cap, cols,
+                                               static_cast<const float*>(d_workspace), d_dbias, d_status,
+                                               (cudaStream_t)stream));
 }
 
 }  // extern "C"
@@ -215,11 +257,11 @@ gq_status check_gemm_common(const int32_t* splits, int32_t G, int64_t rows_cap, 
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
-                        const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
-                        void* y, int32_t out_dtype, int32_t* d_status, gq_stream_t stream)
+gq_status fprop_impl(const gq_quantized* x, const gq_quantized* w, const int32_t* d_split_sizes,
+                     int32_t num_groups, int64_t n, int64_t k, void* y, int32_t out_dtype, const void* d_bias,
+                     int32_t bias_dtype, int32_t* d_status, gq_stream_t stream)
 {
     if (!x || !w)
         return GQ_ERR_INVALID_ARG;
@@ -237,7 +279,34 @@ gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
         return GQ_OK;
     return gq::launch_gemm(gq::GEMM_FPROP, operand(x, false), operand(w, false), d_split_sizes,
                            num_groups, x->rows_cap, n, k, y, out_dtype, 0, d_status,
-                           (cudaStream_t)stream);
+                           (cudaStream_t)stream, nullptr, d_bias, bias_dtype);
+}
+
+}  // namespace
+
+extern "C" {
+
+
+gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
+                        const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                        void* y, int32_t out_dtype, int32_t* d_status, gq_stream_t stream)
+{
+    return fprop_impl(x, w, d_split_sizes, num_groups, n, k, y, out_dtype, nullptr, 0, d_status, stream);
+}
+
+gq_status gq_gemm_fprop_bias(const gq_quantized* x, const gq_quantized* w,
+                             const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                             const void* d_bias, int32_t bias_dtype, void* y, int32_t out_dtype,
+                             int32_t* d_status, gq_stream_t stream)
+{
+    if (!d_bias)
+        return GQ_ERR_INVALID_ARG;
+    if (bias_dtype != GQ_DTYPE_F32 && bias_dtype != GQ_DTYPE_BF16)
+        return GQ_ERR_UNSUPPORTED;
+    if (!aligned16(d_bias))
+        return GQ_ERR_ALIGNMENT;
+    return fprop_impl(x, w, d_split_sizes, num_groups, n, k, y, out_dtype, d_bias, bias_dtype, d_status,
+                      stream);
 }
 
 gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,

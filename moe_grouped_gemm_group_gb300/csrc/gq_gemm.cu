@@ -82,7 +82,36 @@ struct GemmArgs {
     // from the front
     unsigned long long* claim = nullptr;
     int front_ctas = 0;
+    // fprop only: per-group bias [G, n] (fp32, or bf16 when bias_bf16),
+    // added to every live row of the group before the output conversion
+    const void* bias = nullptr;
+    int bias_bf16 = 0;
 };
+
+// Four consecutive bias values of group row `g`, column `col` (col % 4 == 0).
+__device__ __forceinline__ float4 load_bias4(const GemmArgs& p, int g, int64_t col)
+{
+    const int64_t i = (int64_t)g * p.n + col;
+    if (p.bias_bf16) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + i));
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + i));
+}
+
+// v[i] += bias for the 32 columns [col, col + 32) of group g.
+__device__ __forceinline__ void add_bias32(const GemmArgs& p, int g, int64_t col, uint32_t (&v)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 b = load_bias4(p, g, col + i);
+        v[i] = __float_as_uint(__uint_as_float(v[i]) + b.x);
+        v[i + 1] = __float_as_uint(__uint_as_float(v[i + 1]) + b.y);
+        v[i + 2] = __float_as_uint(__uint_as_float(v[i + 2]) + b.z);
+        v[i + 3] = __float_as_uint(__uint_as_float(v[i + 3]) + b.w);
+    }
+}
 
 // Output box slots per epilogue warp of the wide wgrad (tuning knob): more
 // slots keep more of the old main grad in flight per CTA but leave room for
@@ -910,6 +939,9 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             const int32_t ocol = (int32_t)(t.col0 + 128 * h);
 #pragma unroll
             for (int b = 0; b < NBOX; ++b) {
+                // bias of the box's columns, added just before they are converted
+                if (KIND == GEMM_FPROP && p.bias && (OUT_BF16 || (b & 1) == 0))
+                    add_bias32(p, t.g, ocol + 32 * (OUT_BF16 ? b : b >> 1), v[OUT_BF16 ? b : b >> 1]);
                 if (lane == 0)
                     ptx::bulk_wait_read_all();           // the last box's store has read it
                 __syncwarp();
@@ -971,6 +1003,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 ptx::tmem_ld_32x32(base + 32 * cc, v);
                 ptx::tmem_wait_ld(v);
                 if (live) {
+                    if (KIND == GEMM_FPROP && p.bias)
+                        add_bias32(p, t.g, t.col0 + 32 * cc, v);
                     if (OUT_BF16)
                         store_row_bf16(out16 + 32 * cc, v);
                     else
@@ -1557,9 +1591,11 @@ bool make_scale_map(CUtensorMap* map, const void* base, uint64_t bytes)
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
-                      cudaStream_t stream, void* workspace)
+                      cudaStream_t stream, void* workspace, const void* bias, int bias_dtype)
 {
     GemmArgs args;
+    args.bias = bias;
+    args.bias_bf16 = bias_dtype == GQ_DTYPE_BF16;
     args.splits = splits;
     args.G = G;
     args.rows_cap = rows_cap;
@@ -1587,7 +1623,7 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
         const int64_t n_out = kind == GEMM_FPROP ? n : k;
         if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
-        if (kUsePairs && n_out % P_BN == 0 && device_info().sm_count >= 2) {
+        if (kUsePairs && !bias && n_out % P_BN == 0 && device_info().sm_count >= 2) {
             // CTA pairs on 256 x 256 tiles; scale atoms by TMA (rows of 256 bytes)
             CUtensorMap msa, msb;
             const uint64_t sa = std::min<uint64_t>(a.scale_bytes, mx_scale_bytes(G, a.rows, a.cols));

@@ -56,11 +56,16 @@ cudaError_t launch_split_scan(const int32_t* splits, int G, int64_t rows_cap, in
                               cudaStream_t stream);
 cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const int32_t* splits,
                             int G, uint8_t* row_data, uint8_t* row_scale, uint8_t* col_data,
-                            uint8_t* col_scale, int32_t* status, cudaStream_t stream);
+                            uint8_t* col_scale, int32_t* status, cudaStream_t stream, float* dpart = nullptr);
 cudaError_t launch_quant_channel(const void* x, int64_t rows_cap, int64_t cols,
                                  const int32_t* splits, int G, float zero_scale,
                                  uint8_t* col_data, float* col_scale, int32_t* status,
                                  cudaStream_t stream);
+
+// Bias gradient of a grouped buffer from the per-tile column sums that the
+// MX quantiser wrote to dpart (gq_quant.cu).
+cudaError_t launch_dbias_reduce(const int32_t* splits, int G, int64_t rows_cap, int64_t cols,
+                                const float* dpart, float* db, int32_t* status, cudaStream_t stream);
 
 // GEMM launchers (gq_gemm.cu).  Operand buffers are already validated.
 struct GemmOperand {
@@ -75,6 +80,7 @@ enum GemmKind { GEMM_FPROP = 0, GEMM_DGRAD = 1, GEMM_WGRAD_MX = 2, GEMM_WGRAD_CH
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
-                      cudaStream_t stream, void* workspace = nullptr);
+                      cudaStream_t stream, void* workspace = nullptr, const void* bias = nullptr,
+                      int bias_dtype = 0);
 
 }  // namespace gq

@@ -145,8 +145,9 @@ constexpr int kQStageOut = 2 * kQOut + 1024;           // row codes, col codes, 
 constexpr int kQConsumers = 512;                       // 16 consumer warps
 constexpr int kQThreadsMx = kQConsumers + 32;          // + 1 producer warp
 constexpr int kQScanBytes = (GQ_MAX_GROUPS + 1) * 8 + (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 32 * 4;
+constexpr int kQDsum = 2 * 4 * 128 * 4;                // bias-grad column sums [2][4 row blocks][128]
 constexpr int kQSmem = 1024 + kQStages * kQTile + 2 * kQStageOut + 16 * 32 * 4 + 8 * 2 * kQStages + 16 +
-                       kQScanBytes;
+                       kQScanBytes + kQDsum;
 
 // Output tensor maps of k_quant_mx: codes of one orientation as [rows, cols]
 // uint8 with 128-byte swizzle, boxes of 128 columns x 128 rows (whole tiles)
@@ -155,12 +156,14 @@ struct QuantOutMaps {
     CUtensorMap row128, row32, col128, col32;
 };
 
-template <bool ROW, bool COL>
+// DBIAS: also the bias gradient's per-tile column sums of the live rows,
+// written to dpart[global row tile][cols] (fp32, fixed summation order).
+template <bool ROW, bool COL, bool DBIAS>
 __global__ void __launch_bounds__(kQThreadsMx, GQ_Q_MINB)
 k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ QuantOutMaps om,
            int64_t rows_cap, int64_t cols, const int32_t* __restrict__ splits, int G,
            uint8_t* __restrict__ row_scale, uint8_t* __restrict__ col_scale,
-           int32_t* __restrict__ status)
+           float* __restrict__ dpart, int32_t* __restrict__ status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -175,6 +178,7 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
     int32_t* s_tp = reinterpret_cast<int32_t*>(s_off + GQ_MAX_GROUPS + 1);
     int64_t* s_w64 = reinterpret_cast<int64_t*>(s_tp + GQ_MAX_GROUPS + 2);
     int32_t* s_w32 = reinterpret_cast<int32_t*>(s_w64 + 32);
+    float* s_dsum = reinterpret_cast<float*>(s_w32 + 32);               // [2][4][128]
 
     if (load_status(status) != 0)
         return;
@@ -268,6 +272,7 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
                 ptx::mbar_arrive(&empty[s]);
         }
         uint32_t rbyte = 0, cbyte = 0;
+        float csum = 0.f;                                // bias grad: this lane's column over the warp's rows
         if (ok && active) {
             // magnitudes (sign bits cleared), two bf16 per register
             uint32_t mg[16];
@@ -348,7 +353,45 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
                 ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb), make_uint4(w[0], w[1], w[2], w[3]));
                 ptx::sts128(cd_box + ptx::swz128(r_in_tile, 2 * cb + 1), make_uint4(w[4], w[5], w[6], w[7]));
             }
+            if (DBIAS) {
+                // Transposed butterfly: after exchanging half of the remaining
+                // columns with lane ^ 16, ^ 8, ^ 4, ^ 2, ^ 1 (adding what comes
+                // back), lane j holds the sum of column j over the 32 rows, in
+                // an order fixed by the lane bits.
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float send = b4 ? xf[i] : xf[i + 16];
+                    const float keep = b4 ? xf[i + 16] : xf[i];
+                    xf[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float send = b3 ? xf[i] : xf[i + 8];
+                    const float keep = b3 ? xf[i + 8] : xf[i];
+                    xf[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float send = b2 ? xf[i] : xf[i + 4];
+                    const float keep = b2 ? xf[i + 4] : xf[i];
+                    xf[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float send = b1 ? xf[i] : xf[i + 2];
+                    const float keep = b1 ? xf[i + 2] : xf[i];
+                    xf[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                }
+                {
+                    const float send = b0 ? xf[0] : xf[1];
+                    const float keep = b0 ? xf[1] : xf[0];
+                    csum = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                }
+            }
         }
+        if (DBIAS)
+            s_dsum[(it & 1) * 512 + rb * 128 + cb * 32 + lane] = csum;
         // Scale atoms: rowwise (row 32 rb + lane, block cb), columnwise
         // (channel 32 cb + lane, 32-row block rb); inactive warps write the
         // zero entries of a partial last tile.  16 warps cover each atom once.
@@ -359,6 +402,11 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
             ptx::bulk_wait_read_all();      // the previous tile's stores have read their buffer
         if (ptx::named_barrier_or(1, kQConsumers, !ok))
             break;
+        if (DBIAS && threadIdx.x < 128) {
+            // the tile's column sums: its four 32-row blocks, added in order
+            const float* d = s_dsum + (it & 1) * 512 + threadIdx.x;
+            dpart[(s_tp[g] + lt) * cols + ct * 128 + threadIdx.x] = ((d[0] + d[128]) + d[256]) + d[384];
+        }
         if (lead) {
             const int32_t row0 = (int32_t)(s_off[g] + 128 * lt);
             const int32_t x = ct * 128;
@@ -456,6 +504,36 @@ k_quant_ch(const uint16_t* __restrict__ x, int64_t rows_cap, int64_t cols,
     }
 }
 
+// Bias gradient from the per-tile column sums: db[g][c] = sum over the
+// group's row tiles, in tile order, of dpart[tile][c]; empty groups (and
+// L == 0) get 0.
+__global__ void __launch_bounds__(256)
+k_dbias_reduce(const int32_t* __restrict__ splits, int G, int64_t rows_cap, int64_t cols,
+               const float* __restrict__ dpart, float* __restrict__ db, int32_t* __restrict__ status)
+{
+    __shared__ int64_t s_off[GQ_MAX_GROUPS + 1];
+    __shared__ int32_t s_tp[GQ_MAX_GROUPS + 1];
+    __shared__ int64_t s_w64[32];
+    __shared__ int32_t s_w32[32];
+    if (load_status(status) != 0)
+        return;
+    const int err = block_scan_splits(splits, G, rows_cap, 32, s_off, s_tp, s_w64, s_w32);
+    if (err) {
+        if (threadIdx.x == 0)
+            set_status(status, err);
+        return;
+    }
+    const int64_t n = (int64_t)G * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int g = (int)(i / cols);
+        const int64_t c = i - (int64_t)g * cols;
+        float acc = 0.f;
+        for (int64_t t = s_tp[g]; t < s_tp[g + 1]; ++t)
+            acc += dpart[t * cols + c];
+        db[i] = acc;
+    }
+}
+
 int blocks_per_sm_for(const void* fn, int threads)
 {
     int n = 1;
@@ -477,7 +555,7 @@ cudaError_t launch_split_scan(const int32_t* splits, int G, int64_t rows_cap, in
 
 cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const int32_t* splits,
                             int G, uint8_t* row_data, uint8_t* row_scale, uint8_t* col_data,
-                            uint8_t* col_scale, int32_t* status, cudaStream_t stream)
+                            uint8_t* col_scale, int32_t* status, cudaStream_t stream, float* dpart)
 {
     CUtensorMap map;
     QuantOutMaps om;
@@ -498,14 +576,31 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows_cap, int64_t cols, const
             return e;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, tiles_bound));
         kernel<<<(unsigned)grid, kQThreadsMx, kQSmem, stream>>>(map, om, rows_cap, cols, splits, G, row_scale,
-                                                                col_scale, status);
+                                                                col_scale, dpart, status);
         return cudaGetLastError();
     };
+    if (dpart) {
+        if (row_data && col_data)
+            return go(k_quant_mx<true, true, true>);
+        if (row_data)
+            return go(k_quant_mx<true, false, true>);
+        return go(k_quant_mx<false, true, true>);
+    }
     if (row_data && col_data)
-        return go(k_quant_mx<true, true>);
+        return go(k_quant_mx<true, true, false>);
     if (row_data)
-        return go(k_quant_mx<true, false>);
-    return go(k_quant_mx<false, true>);
+        return go(k_quant_mx<true, false, false>);
+    return go(k_quant_mx<false, true, false>);
+}
+
+cudaError_t launch_dbias_reduce(const int32_t* splits, int G, int64_t rows_cap, int64_t cols,
+                                const float* dpart, float* db, int32_t* status, cudaStream_t stream)
+{
+    const int64_t n = (int64_t)G * cols;
+    const int64_t cap = (int64_t)device_info().sm_count * 4;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, cap));
+    k_dbias_reduce<<<grid, 256, 0, stream>>>(splits, G, rows_cap, cols, dpart, db, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quant_channel(const void* x, int64_t rows_cap, int64_t cols,

@@ -18,6 +18,8 @@ larger than the 129 MB L2):
   wgrad       moe_e8 fc1 k-grouped wgrad accumulating into fp32 (8 x 2048 x 4096)
   wgrad64     moe_e64_zipf fc1 k-grouped wgrad accumulating into fp32
               (64 x 2048 x 7168; 3.8 GB main grad)
+  fprop_bias  fprop with a bf16 per-group bias added in the epilogue
+  quant_dbias quant fused with the per-group bias gradient (its column sums)
 Options: --uniform replaces the workload's splits by the uniform split of
 the same live total; --store writes the wgrad result (accumulate = 0)
 instead of adding it to the main grad; --static runs the wgrad in its static
@@ -39,7 +41,7 @@ if ROOT not in sys.path:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad64",
-                                     "wgrad_ch"])
+                                     "wgrad_ch", "fprop_bias", "quant_dbias"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--uniform", action="store_true")
     ap.add_argument("--store", action="store_true")
@@ -73,6 +75,20 @@ def main():
         x = W.device_activation(w, H, 0, device=dev)
         q = gq.alloc_quantized(R, H, E, mx, dev)
         fn = lambda: gq.gq_quantize(x, sp, E, mx, q, st)  # noqa: E731
+    elif args.case == "quant_dbias":
+        x = W.device_activation(w, H, 0, device=dev)
+        q = gq.alloc_quantized(R, H, E, mx, dev)
+        db = torch.empty((E, H), device=dev)
+        wsd = torch.empty(gq.gq_dbias_workspace_bytes(E, R, H), dtype=torch.uint8, device=dev)
+        fn = lambda: gq.gq_quantize_dbias(x, sp, E, mx, q, db, wsd, st)  # noqa: E731
+    elif args.case == "fprop_bias":
+        wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
+        qw = quant(wt, None)
+        del wt
+        qx = quant(W.device_activation(w, H, 0, device=dev), sp)
+        bias = W.device_normal_bf16((E, F), w.seed, 0.5, 30, dev)
+        y = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
+        fn = lambda: gq.gq_gemm_fprop_bias(qx, qw, sp, E, F, H, bias, y, gq.DTYPE_BF16, st)  # noqa: E731
     elif args.case in ("fprop", "dgrad", "fprop2", "dgrad2"):
         # fc1: Y = X W1^T with n = ffn, k = hidden; fc2: n = hidden, k = ffn
         n, k = (F, H) if args.case in ("fprop", "dgrad") else (H, F)

@@ -126,6 +126,28 @@ def test_noalloc_wgrad_refuses_too_many_tiles_without_a_gpu(lib):
     assert lib.gq_gemm_wgrad_noalloc(None, None, None, 1024, 1 << 17, 1 << 19, None, 1, None, None) == -1
 
 
+def test_bias_entry_points_host_checks_need_no_gpu(lib):
+    st = C.c_void_p(0x20000)
+    out = C.c_void_p(0x30000)
+    x = _desc(1, 256, 256, row=1, col=0)
+    x.row_data, x.row_scale, x.row_scale_bytes = 0x40000, 0x50000, 1 << 20
+    w = _desc(1, 128, 256, row=1, col=0)
+    w.row_data, w.row_scale, w.row_scale_bytes = 0x60000, 0x70000, 1 << 20
+    # no bias, a bias dtype that is neither fp32 nor bf16, a misaligned bias
+    assert lib.gq_gemm_fprop_bias(C.byref(x), C.byref(w), None, 1, 128, 256, None, 0, out, 0, st, None) == -1
+    assert lib.gq_gemm_fprop_bias(C.byref(x), C.byref(w), None, 1, 128, 256, C.c_void_p(0x80000), 5, out, 0,
+                                  st, None) == -4
+    assert lib.gq_gemm_fprop_bias(C.byref(x), C.byref(w), None, 1, 128, 256, C.c_void_p(0x80004), 0, out, 0,
+                                  st, None) == -2
+    # bias-grad workspace: the bound, and a refusal below it
+    assert gq.gq_dbias_workspace_bytes(4, 1024, 256) == 4 * 256 * (8 + 4)
+    assert gq.gq_dbias_workspace_bytes(4, 1024, 200) == 0
+    mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    d = _desc(1, 256, 256)
+    assert lib.gq_quantize_dbias(C.c_void_p(0x10000), 256, 256, None, 1, C.byref(mx), C.byref(d),
+                                 C.c_void_p(0x90000), C.c_void_p(0xa0000), 16, st, None) == -1
+
+
 def test_binding_refuses_host_tensors(lib):
     torch = pytest.importorskip("torch")
     x = torch.zeros((128, 128), dtype=torch.bfloat16)
