@@ -78,7 +78,10 @@ def _load():
                                                 C.c_int64]
             lib.or_grouped_bias_grad.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int64, C.c_int64,
                                                  C.c_void_p]
-            for name in ("or_split_scan", "or_quantize_mx", "or_quantize_channel",
+            lib.or_srelu_quantize_mx.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                                 C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p,
+                                                 C.c_void_p, C.c_int64]
+            for name in ("or_split_scan", "or_quantize_mx", "or_quantize_channel", "or_srelu_quantize_mx",
                          "or_gemm_fprop", "or_gemm_dgrad", "or_gemm_wgrad_mx",
                          "or_gemm_wgrad_channel", "or_gemm_sample", "or_grouped_bias_add",
                          "or_grouped_bias_grad"):
@@ -187,6 +190,26 @@ def quantize_mx(x_bits, splits, num_groups: int, rowwise=True, colwise=True,
     st = lib.or_quantize_mx(_p(x), R, Cc, _p(s), num_groups, int(rowwise), int(colwise),
                             _p(rd), _p(rs), cap, _p(cd), _p(cs), cap)
     _check(st, "quantize_mx")
+    return MXQuantized(rd, rs, cd, cs, s, R, Cc)
+
+
+def srelu_quantize_mx(y: np.ndarray, probs: np.ndarray, splits, num_groups: int, data_fill: int = 0,
+                      scale_fill: int = 0) -> MXQuantized:
+    """ScaledSReLU of an fp32 [R, C] buffer, a = probs[r] * relu(y)^2 in fp32,
+    then MXFP8 1x32 quantisation rowwise and columnwise (as quantize_mx)."""
+    lib = _load()
+    yy = np.ascontiguousarray(y, np.float32)
+    pr = np.ascontiguousarray(probs, np.float32)
+    R, Cc = yy.shape
+    s = _splits(splits)
+    need = int(split_scan(s, num_groups, R, Cc)[2][-1])
+    rd = np.full((R, Cc), data_fill, np.uint8)
+    cd = np.full((R, Cc), data_fill, np.uint8)
+    rs = np.full(max(need, 1), scale_fill, np.uint8)
+    cs = np.full(max(need, 1), scale_fill, np.uint8)
+    st = lib.or_srelu_quantize_mx(_p(yy), _p(pr), R, Cc, _p(s), num_groups, _p(rd), _p(rs), need, _p(cd),
+                                  _p(cs), need)
+    _check(st, "srelu_quantize_mx")
     return MXQuantized(rd, rs, cd, cs, s, R, Cc)
 
 

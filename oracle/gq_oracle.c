@@ -691,3 +691,90 @@ int or_grouped_bias_grad(const uint16_t* dy, const int32_t* splits, int G, int64
         }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* ScaledSReLU + MXFP8 quantisation of an fp32 activation                    */
+/* ------------------------------------------------------------------------ */
+
+/* a = probs[r] * relu(y)^2 in fp32, op by op: t = max(y, 0); t = t * t;
+ * a = t * probs[r] (the ScaledSReLU between fc1 and fc2 in TransformerEngine
+ * issue 3484's reproducer, te.ops.ScaledSReLU, fed with per-token probs;
+ * the pages name it without printing its arithmetic: squared ReLU scaled by
+ * the row's prob is the plain reading).  Then MXFP8 1x32 quantisation of the
+ * fp32 values, rowwise and columnwise, with the same scale rule, codes and
+ * swizzled scale layout as or_quantize_mx.  Rows past the live total are
+ * neither read nor written. */
+int or_srelu_quantize_mx(const float* y, const float* probs, int64_t rows_cap, int64_t cols,
+                         const int32_t* splits, int G, uint8_t* row_data, uint8_t* row_scale,
+                         int64_t row_scale_bytes, uint8_t* col_data, uint8_t* col_scale,
+                         int64_t col_scale_bytes)
+{
+    int64_t *off = malloc(sizeof(int64_t) * (G + 1) * 3);
+    int64_t *tp, *sb, L;
+    float* a;
+    int st;
+    if (!off)
+        return OR_ERR_INVALID_ARG;
+    tp = off + (G + 1);
+    sb = off + 2 * (G + 1);
+    st = or_split_scan(splits, G, rows_cap, cols, OR_RECIPE_MX, off, tp, sb);
+    if (st != OR_OK) {
+        free(off);
+        return st;
+    }
+    if (sb[G] > row_scale_bytes || sb[G] > col_scale_bytes) {
+        free(off);
+        return OR_ERR_INVALID_ARG;
+    }
+    L = off[G];
+    a = malloc(sizeof(float) * (size_t)(L > 0 ? L * cols : 1));
+    if (!a) {
+        free(off);
+        return OR_ERR_INVALID_ARG;
+    }
+    for (int64_t r = 0; r < L; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float t = y[r * cols + c];
+            t = t > 0.0f ? t : 0.0f;
+            t = t * t;
+            a[r * cols + c] = t * probs[r];
+        }
+    memset(row_scale, 0, (size_t)sb[G]);
+    memset(col_scale, 0, (size_t)sb[G]);
+    for (int g = 0; g < G; ++g) {
+        int64_t o = off[g], m = off[g + 1] - off[g], T = tp[g + 1] - tp[g];
+#pragma omp parallel for schedule(static)
+        for (int64_t lr = 0; lr < m; ++lr) {
+            int64_t r = o + lr;
+            for (int64_t j = 0; j < cols / 32; ++j) {
+                double amax = 0.0;
+                int e;
+                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
+                    if (fabs((double)a[r * cols + c]) > amax)
+                        amax = fabs((double)a[r * cols + c]);
+                e = or_mx_scale_exponent(amax);
+                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
+                    row_data[r * cols + c] = or_e4m3_encode(ldexp((double)a[r * cols + c], -e));
+                row_scale[sb[g] + ((lr / 128) * (cols / 128) + j / 4) * 512 + atom_byte(lr % 128, j % 4)] =
+                    (uint8_t)(e + 127);
+            }
+        }
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; ++c) {
+            for (int64_t b = 0; b < m / 32; ++b) {
+                double amax = 0.0;
+                int e;
+                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
+                    if (fabs((double)a[(o + lr) * cols + c]) > amax)
+                        amax = fabs((double)a[(o + lr) * cols + c]);
+                e = or_mx_scale_exponent(amax);
+                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
+                    col_data[(o + lr) * cols + c] = or_e4m3_encode(ldexp((double)a[(o + lr) * cols + c], -e));
+                col_scale[sb[g] + ((c / 128) * T + b / 4) * 512 + atom_byte(c % 128, b % 4)] = (uint8_t)(e + 127);
+            }
+        }
+    }
+    free(a);
+    free(off);
+    return OR_OK;
+}
