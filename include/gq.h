@@ -226,6 +226,33 @@ gq_status gq_gemm_fprop_bias(const gq_quantized* x, const gq_quantized* w,
                              int32_t* d_status, gq_stream_t stream);
 
 /*
+ * gq_gemm_fprop_srelu_quant -- the fc1 forward with the activation and the
+ * quantisation of fc2's input fused into the GEMM's epilogue: Y_g = X_g W_g^T
+ * (+ b_g), and the MXFP8 rowwise and columnwise quantisation of
+ *   A[r, c] = probs[r] * relu(Y[r, c])^2
+ * computed from the fp32 accumulator (t = max(y, 0); t = t * t; a = t * p,
+ * fp32 op by op), so A never exists in bf16 or in HBM.  This is the fc1 ->
+ * ScaledSReLU -> fc2 sequence of TransformerEngine issue 3484's reproducer
+ * (te.ops.ScaledSReLU fed with per-token probs); the pages name the
+ * activation without printing it, and squared ReLU times the row's prob is
+ * the plain reading.
+ *   d_bias  : NULL, or as gq_gemm_fprop_bias (added before the activation).
+ *   d_probs : fp32 [R] device array, 16-byte aligned (only rows < L read).
+ *   y       : [R, n] of out_dtype, the pre-activation result (what the
+ *             activation's backward needs), as gq_gemm_fprop.
+ *   act_out : an MX descriptor with rowwise and colwise buffers, num_groups,
+ *             rows_cap = x's rows_cap, cols = n; filled exactly as
+ *             gq_quantize would fill it from A (same scale rule, codes,
+ *             swizzled grouped atoms, zero entries past each group's end).
+ * n must be a multiple of 256 (GQ_ERR_UNSUPPORTED otherwise).
+ */
+gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w,
+                                    const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                                    const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
+                                    int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                                    gq_stream_t stream);
+
+/*
  * gq_gemm_dgrad -- dX_g = dY_g W_g (TransformerEngine issue 3484: M is a
  * free dimension of the dgrad).
  *   dy : MX rowwise, rows_cap R, cols n.

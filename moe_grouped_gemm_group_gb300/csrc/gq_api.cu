@@ -261,7 +261,8 @@ namespace {
 
 gq_status fprop_impl(const gq_quantized* x, const gq_quantized* w, const int32_t* d_split_sizes,
                      int32_t num_groups, int64_t n, int64_t k, void* y, int32_t out_dtype, const void* d_bias,
-                     int32_t bias_dtype, int32_t* d_status, gq_stream_t stream)
+                     int32_t bias_dtype, int32_t* d_status, gq_stream_t stream,
+                     const gq::ActOutput* act = nullptr)
 {
     if (!x || !w)
         return GQ_ERR_INVALID_ARG;
@@ -279,7 +280,7 @@ gq_status fprop_impl(const gq_quantized* x, const gq_quantized* w, const int32_t
         return GQ_OK;
     return gq::launch_gemm(gq::GEMM_FPROP, operand(x, false), operand(w, false), d_split_sizes,
                            num_groups, x->rows_cap, n, k, y, out_dtype, 0, d_status,
-                           (cudaStream_t)stream, nullptr, d_bias, bias_dtype);
+                           (cudaStream_t)stream, nullptr, d_bias, bias_dtype, act);
 }
 
 }  // namespace
@@ -307,6 +308,40 @@ gq_status gq_gemm_fprop_bias(const gq_quantized* x, const gq_quantized* w,
         return GQ_ERR_ALIGNMENT;
     return fprop_impl(x, w, d_split_sizes, num_groups, n, k, y, out_dtype, d_bias, bias_dtype, d_status,
                       stream);
+}
+
+gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w,
+                                    const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                                    const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
+                                    int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                                    gq_stream_t stream)
+{
+    if (!x || !act_out || !d_probs)
+        return GQ_ERR_INVALID_ARG;
+    if (d_bias && bias_dtype != GQ_DTYPE_F32 && bias_dtype != GQ_DTYPE_BF16)
+        return GQ_ERR_UNSUPPORTED;
+    if ((d_bias && !aligned16(d_bias)) || !aligned16(d_probs))
+        return GQ_ERR_ALIGNMENT;
+    if (n % 256 != 0)
+        return GQ_ERR_UNSUPPORTED;
+    if (act_out->num_groups != num_groups || act_out->rows_cap != x->rows_cap || act_out->cols != n)
+        return GQ_ERR_SHAPE_MISMATCH;
+    if (act_out->recipe.kind != GQ_RECIPE_MXFP8_1X32 || !act_out->recipe.rowwise || !act_out->recipe.colwise)
+        return GQ_ERR_UNSUPPORTED;
+    if (x->rows_cap > 0) {
+        if (!act_out->row_data || !act_out->row_scale || !act_out->col_data || !act_out->col_scale)
+            return GQ_ERR_INVALID_ARG;
+        if (!aligned16(act_out->row_data) || !aligned16(act_out->row_scale) || !aligned16(act_out->col_data) ||
+            !aligned16(act_out->col_scale))
+            return GQ_ERR_ALIGNMENT;
+        const uint64_t need = mx_scale_bound(num_groups, x->rows_cap, n);
+        if (act_out->row_scale_bytes < need || act_out->col_scale_bytes < need)
+            return GQ_ERR_INVALID_ARG;
+    }
+    const gq::ActOutput act{d_probs, (uint8_t*)act_out->row_data, (uint8_t*)act_out->row_scale,
+                            (uint8_t*)act_out->col_data, (uint8_t*)act_out->col_scale};
+    return fprop_impl(x, w, d_split_sizes, num_groups, n, k, y, out_dtype, d_bias, bias_dtype, d_status, stream,
+                      &act);
 }
 
 gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,

@@ -31,6 +31,7 @@
 // tokens, padding, or out-of-range zero fill) never enter a contraction.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -86,6 +87,14 @@ struct GemmArgs {
     // added to every live row of the group before the output conversion
     const void* bias = nullptr;
     int bias_bf16 = 0;
+    // fprop with the fused activation (the ACT kernels): per-row probs, and
+    // the MXFP8 rowwise / columnwise codes [R, n] and grouped swizzled scale
+    // atoms of probs[r] * relu(y)^2
+    const float* act_probs = nullptr;
+    uint8_t* act_row = nullptr;
+    uint8_t* act_row_scale = nullptr;
+    uint8_t* act_col = nullptr;
+    uint8_t* act_col_scale = nullptr;
 };
 
 // Four consecutive bias values of group row `g`, column `col` (col % 4 == 0).
@@ -390,6 +399,130 @@ __device__ __forceinline__ int64_t ring_get(uint64_t* full, uint64_t* empty, con
     return tile;
 }
 
+// E8M0 byte of a block from its fp32 amax: max(E - 8, 0) with E the biased
+// exponent field (floor(log2 amax) - 8, clamped at -127; zero and subnormal
+// amax give 0), and 2^-e for that byte as an exact fp32 power of two.
+__device__ __forceinline__ uint32_t e8m0_of_f32(float amax)
+{
+    const int E = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+    return (uint32_t)max(E - 8, 0);
+}
+
+__device__ __forceinline__ float inv_scale_of(uint32_t byte) { return __uint_as_float((254u - byte) << 23); }
+
+// Four e4m3 codes (x0's in the low byte) of x * s, rounded to nearest even
+// and saturated; the products are exact (s is a power of two).
+__device__ __forceinline__ uint32_t codes4(float x0, float x1, float x2, float x3, float s0, float s1, float s2,
+                                          float s3)
+{
+    const float2 lo = __fmul2_rn(make_float2(x0, x1), make_float2(s0, s1));
+    const float2 hi = __fmul2_rn(make_float2(x2, x3), make_float2(s2, s3));
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3) |
+           ((uint32_t)__nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3) << 16);
+}
+
+// The fused activation of one epilogue warp: its 32 rows (lane = row, one
+// 32-row block of the group) x 128 columns of the fp32 result in v.
+// a = probs[r] * relu(y)^2 in fp32 (t = max(y, 0); t = t * t; a = t * p),
+// then MXFP8 1x32 codes and E8M0 scales of a, rowwise (blocks of 32 columns)
+// and columnwise (the warp's 32 rows), written to the grouped layout of a
+// [R, n] buffer: atoms of group g at 512 * (n/128) * (tiles before g),
+// rowwise [row tile][column block], columnwise [column block][row tile],
+// byte (r % 32) * 16 + (r / 32) * 4 + j.  A warp whose rows lie past the
+// group's end writes the zero entries of its atoms and nothing else.
+template <int BN>
+__device__ __forceinline__ void act_quant_warp(const GemmArgs& p, const Tile& t, const int32_t* s_tp, int q,
+                                               int h, int lane, bool live, uint32_t (&v)[4][32])
+{
+    const int64_t nb = p.n / 128;
+    const int64_t cb = (t.col0 + 128 * h) / 128;
+    const int64_t sb = 512 * nb * (int64_t)s_tp[t.g];
+    uint8_t* ratom = p.act_row_scale + sb + (t.mt * nb + cb) * 512;
+    uint8_t* catom = p.act_col_scale + sb + (cb * t.T + t.mt) * 512;
+    if (!live) {
+        *reinterpret_cast<uint32_t*>(ratom + lane * 16 + q * 4) = 0u;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+            catom[lane * 16 + cc * 4 + q] = 0;
+        return;
+    }
+    const int64_t row = t.row0 + 32 * q + lane;
+    const float pr = __ldg(p.act_probs + row);
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+    uint32_t rword = 0;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int64_t col = t.col0 + 128 * h + 32 * cc;
+        uint32_t amax_r = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float x = __uint_as_float(v[cc][i]);
+            x = x > 0.f ? x : 0.f;
+            const float a = __fmul_rn(__fmul_rn(x, x), pr);
+            v[cc][i] = __float_as_uint(a);
+            amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
+        }
+        // rowwise
+        const uint32_t rb = e8m0_of_f32(__uint_as_float(amax_r));
+        const float rs = inv_scale_of(rb);
+        rword |= rb << (8 * cc);
+        {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]), rs, rs, rs, rs);
+            uint4* dst = reinterpret_cast<uint4*>(p.act_row + row * p.n + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        // columnwise: transposed butterfly max over the 32 rows (lane j ends
+        // with column j), on the magnitudes' bit patterns
+        uint32_t m[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t send = (b4 ? v[cc][i] : v[cc][i + 16]) & 0x7fffffffu;
+            const uint32_t keep = (b4 ? v[cc][i + 16] : v[cc][i]) & 0x7fffffffu;
+            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t send = b3 ? m[i] : m[i + 8];
+            const uint32_t keep = b3 ? m[i + 8] : m[i];
+            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t send = b2 ? m[i] : m[i + 4];
+            const uint32_t keep = b2 ? m[i + 4] : m[i];
+            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t send = b1 ? m[i] : m[i + 2];
+            const uint32_t keep = b1 ? m[i + 2] : m[i];
+            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+        }
+        const uint32_t colmax = max(b0 ? m[1] : m[0], __shfl_xor_sync(0xffffffffu, b0 ? m[0] : m[1], 1));
+        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(colmax));
+        catom[lane * 16 + cc * 4 + q] = (uint8_t)cbyte;
+        const float csc = inv_scale_of(cbyte);
+        {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]),
+                              __shfl_sync(0xffffffffu, csc, 4 * i), __shfl_sync(0xffffffffu, csc, 4 * i + 1),
+                              __shfl_sync(0xffffffffu, csc, 4 * i + 2), __shfl_sync(0xffffffffu, csc, 4 * i + 3));
+            uint4* dst = reinterpret_cast<uint4*>(p.act_col + row * p.n + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+    *reinterpret_cast<uint32_t*>(ratom + lane * 16 + q * 4) = rword;
+}
+
 // Wait for the TMA writes of the last min(stages, issued) issued stages, so
 // that none lands after the CTA has left (bounded; used on every exit path).
 __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t issued,
@@ -405,7 +538,9 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t 
 // MXFP8 grouped GEMM (fprop, dgrad, wgrad)                                  //
 // ------------------------------------------------------------------------ //
 
-template <int KIND, int BN, bool OUT_BF16>
+// ACT (fprop, BN = 256 only): the epilogue also writes the MX-quantised
+// ScaledSReLU of the result (act_quant_warp).
+template <int KIND, int BN, bool OUT_BF16, bool ACT = false>
 __global__ void __launch_bounds__(MxShape<KIND, BN>::THREADS, 1)
 k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
           const __grid_constant__ CUtensorMap tma_o, const GemmArgs p)
@@ -933,8 +1068,11 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (lane == 0)
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
-            if (32 * q >= t.rows)
+            if (32 * q >= t.rows) {
+                if constexpr (ACT)
+                    act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, false, v);
                 continue;
+            }
             const int32_t orow = (int32_t)(t.row0 + 32 * q);
             const int32_t ocol = (int32_t)(t.col0 + 128 * h);
 #pragma unroll
@@ -971,6 +1109,8 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     ptx::bulk_commit_group();
                 }
             }
+            if constexpr (ACT)
+                act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, true, v);
         }
         if (lane == 0)
             ptx::bulk_wait_all();
@@ -1531,12 +1671,12 @@ cudaError_t prepare(Kernel kernel, int smem)
     return prepare_kernel(reinterpret_cast<const void*>(kernel), smem, 0, nullptr);
 }
 
-template <int KIND, int BN, bool OUT_BF16>
+template <int KIND, int BN, bool OUT_BF16, bool ACT = false>
 gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                  const GemmArgs& args, int64_t tiles_bound, cudaStream_t stream)
 {
     using S = MxShape<KIND, BN>;
-    auto kernel = k_gemm_mx<KIND, BN, OUT_BF16>;
+    auto kernel = k_gemm_mx<KIND, BN, OUT_BF16, ACT>;
     if (prepare(kernel, S::SMEM) != cudaSuccess)
         return GQ_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_bound, device_info().sm_count));
@@ -1591,11 +1731,19 @@ bool make_scale_map(CUtensorMap* map, const void* base, uint64_t bytes)
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
-                      cudaStream_t stream, void* workspace, const void* bias, int bias_dtype)
+                      cudaStream_t stream, void* workspace, const void* bias, int bias_dtype,
+                      const ActOutput* act)
 {
     GemmArgs args;
     args.bias = bias;
     args.bias_bf16 = bias_dtype == GQ_DTYPE_BF16;
+    if (act) {
+        args.act_probs = act->probs;
+        args.act_row = act->row_data;
+        args.act_row_scale = act->row_scale;
+        args.act_col = act->col_data;
+        args.act_col_scale = act->col_scale;
+    }
     args.splits = splits;
     args.G = G;
     args.rows_cap = rows_cap;
@@ -1623,7 +1771,9 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
         const int64_t n_out = kind == GEMM_FPROP ? n : k;
         if (!make_map_u8(&ma, a.data, a.rows, a.cols, 128) || !make_map_u8(&mb, b.data, b.rows, b.cols, 128))
             return GQ_ERR_CUDA;
-        if (kUsePairs && !bias && n_out % P_BN == 0 && device_info().sm_count >= 2) {
+        if (act && (kind != GEMM_FPROP || !kWideTiles || n_out % 256 != 0))
+            return GQ_ERR_UNSUPPORTED;
+        if (kUsePairs && !bias && !act && n_out % P_BN == 0 && device_info().sm_count >= 2) {
             // CTA pairs on 256 x 256 tiles; scale atoms by TMA (rows of 256 bytes)
             CUtensorMap msa, msb;
             const uint64_t sa = std::min<uint64_t>(a.scale_bytes, mx_scale_bytes(G, a.rows, a.cols));
@@ -1648,6 +1798,9 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                                          bf16 ? 2 : 4, out, rows_cap, n_out, bf16 ? 32 : 16, 32))
                 return GQ_ERR_CUDA;
             const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 256);
+            if (kind == GEMM_FPROP && act)
+                return bf16 ? run_mx<GEMM_FPROP, 256, true, true>(ma, mb, mo, args, bound, stream)
+                            : run_mx<GEMM_FPROP, 256, false, true>(ma, mb, mo, args, bound, stream);
             if (kind == GEMM_FPROP)
                 return bf16 ? run_mx<GEMM_FPROP, 256, true>(ma, mb, mo, args, bound, stream)
                             : run_mx<GEMM_FPROP, 256, false>(ma, mb, mo, args, bound, stream);

@@ -77,10 +77,20 @@ struct GemmOperand {
 };
 enum GemmKind { GEMM_FPROP = 0, GEMM_DGRAD = 1, GEMM_WGRAD_MX = 2, GEMM_WGRAD_CHANNEL = 3 };
 
+// Outputs of the fprop with the fused ScaledSReLU + MX quantisation: per-row
+// probs and the MX rowwise / columnwise codes and scales of the activation.
+struct ActOutput {
+    const float* probs;
+    uint8_t* row_data;
+    uint8_t* row_scale;
+    uint8_t* col_data;
+    uint8_t* col_scale;
+};
+
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,
                       cudaStream_t stream, void* workspace = nullptr, const void* bias = nullptr,
-                      int bias_dtype = 0);
+                      int bias_dtype = 0, const ActOutput* act = nullptr);
 
 }  // namespace gq

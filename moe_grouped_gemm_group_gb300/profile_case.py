@@ -20,6 +20,8 @@ larger than the 129 MB L2):
               (64 x 2048 x 7168; 3.8 GB main grad)
   fprop_bias  fprop with a bf16 per-group bias added in the epilogue
   quant_dbias quant fused with the per-group bias gradient (its column sums)
+  fprop_act   fc1 fprop with ScaledSReLU + MX row/col quantisation of the
+              activation fused into the epilogue (bf16 pre-activation out)
 Options: --uniform replaces the workload's splits by the uniform split of
 the same live total; --store writes the wgrad result (accumulate = 0)
 instead of adding it to the main grad; --static runs the wgrad in its static
@@ -41,7 +43,7 @@ if ROOT not in sys.path:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad64",
-                                     "wgrad_ch", "fprop_bias", "quant_dbias"])
+                                     "wgrad_ch", "fprop_bias", "quant_dbias", "fprop_act"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--uniform", action="store_true")
     ap.add_argument("--store", action="store_true")
@@ -81,6 +83,16 @@ def main():
         db = torch.empty((E, H), device=dev)
         wsd = torch.empty(gq.gq_dbias_workspace_bytes(E, R, H), dtype=torch.uint8, device=dev)
         fn = lambda: gq.gq_quantize_dbias(x, sp, E, mx, q, db, wsd, st)  # noqa: E731
+    elif args.case == "fprop_act":
+        wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
+        qw = quant(wt, None)
+        del wt
+        qx = quant(W.device_activation(w, H, 0, device=dev), sp)
+        probs = torch.rand(R, device=dev)
+        y = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
+        qa = gq.alloc_quantized(R, F, E, mx, dev)
+        fn = lambda: gq.gq_gemm_fprop_srelu_quant(qx, qw, sp, E, F, H, probs, y, gq.DTYPE_BF16, qa,  # noqa: E731
+                                                  st)
     elif args.case == "fprop_bias":
         wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
         qw = quant(wt, None)
