@@ -96,6 +96,9 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay measurement of the step")
     ap.add_argument("--json-out", default=None)
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step: the single grouped weight quantisation and the token-count "
+                         "sweep (hidden 4096, 32 experts, expert width 1536), as a table")
     return ap.parse_args()
 
 
@@ -497,9 +500,94 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
+def _event_ms(fn, reps: int = 20, warm: int = 3) -> float:
+    """Median CUDA-event time of fn() over `reps` launches after `warm`."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in ms]))
+
+
+def run_sweep(peaks):
+    """The single-grouped-weight quantisation (128 experts x [4096, 1536] in
+    one buffer, uniform split, quantised twice into one reused output) and
+    the token-count sweep T = 1K .. 256K at hidden 4096 over 32 uniform
+    experts with expert width 1536: quantiser GB/s and fprop / dgrad / wgrad
+    TFLOP/s, CUDA-event medians, against the measured peaks."""
+    import torch
+
+    import moe_grouped_gemm_group_gb300 as gq
+    import workloads as W
+    dev = "cuda:0"
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks["bf16_tflops"]) * MXFP8_OVER_BF16
+    mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lines = ["| case | quantise X ms (GB/s, frac) | fprop ms (TFLOP/s, frac) | dgrad ms (TFLOP/s) | "
+             "wgrad ms (TFLOP/s, GB/s) |", "|---|---|---|---|---|"]
+    sw = W.workload("single_grouped_weight")
+    wbuf = W.device_normal_bf16((sw.rows_cap, sw.hidden), sw.seed, 0.02, 0, dev)
+    qw = gq.alloc_quantized(sw.rows_cap, sw.hidden, sw.num_groups, mx, dev)
+    t = _event_ms(lambda: gq.gq_quantize(wbuf, None, sw.num_groups, mx, qw, st))
+    gbs = 4.0625 * wbuf.numel() / (t * 1e-3) / 1e9
+    lines.append(f"| single grouped weight 128 x [4096, 1536] | {t:.3f} ({gbs:.0f}, {gbs / hbm:.2f}) | | | |")
+    del wbuf, qw
+    E, H, N = 32, 4096, 1536
+    w = W.device_normal_bf16((E * N, H), 6, 0.02, 1, dev)
+    qw = gq.alloc_quantized(E * N, H, E, mx, dev)
+    gq.gq_quantize(w, None, E, mx, qw, st)
+    dw = torch.zeros((E, N, H), device=dev)
+    ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+    for T in W.SWEEP_TOKENS:
+        wl = W.workload("token_sweep", tokens=T)
+        sp = torch.as_tensor(wl.splits).to(dev)
+        x = W.device_normal_bf16((T, H), wl.seed, 1.0, 2, dev)
+        dy = W.device_normal_bf16((T, N), wl.seed, 1.0, 3, dev)
+        qx = gq.alloc_quantized(T, H, E, mx, dev)
+        qd = gq.alloc_quantized(T, N, E, mx, dev)
+        gq.gq_quantize(dy, sp, E, mx, qd, st)
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        tq = _event_ms(lambda: gq.gq_quantize(x, sp, E, mx, qx, st))
+        tf = _event_ms(lambda: gq.gq_gemm_fprop(qx, qw, sp, E, N, H, y, gq.DTYPE_BF16, st))
+        td = _event_ms(lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, N, H, dx, gq.DTYPE_BF16, st))
+        tw = _event_ms(lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, N, H, dw, True, st, workspace=ws))
+        flops = 2.0 * T * N * H
+        gbs = 4.0625 * T * H / (tq * 1e-3) / 1e9
+        tff, tfd, tfw = (flops / (v * 1e-3) / 1e12 for v in (tf, td, tw))
+        wbytes = T * (N + H) * (1 + 1 / 32) + E * N * H * 8.0
+        lines.append(f"| T = {T // 1024}K | {tq:.3f} ({gbs:.0f}, {gbs / hbm:.2f}) | {tf:.3f} ({tff:.0f}, "
+                     f"{tff / tc:.2f}) | {td:.3f} ({tfd:.0f}) | {tw:.3f} ({tfw:.0f}, "
+                     f"{wbytes / (tw * 1e-3) / 1e9:.0f}) |")
+        del x, dy, qx, qd, y, dx
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise SystemExit(f"device status {int(st.item())} in the sweep")
+    print("\n".join(lines))
+
+
 def main():
     args = parse_args()
     dist = Dist(args.gpus)
+    if args.sweep:
+        import torch
+        torch.cuda.set_device(dist.local)
+        import moe_grouped_gemm_group_gb300 as gq
+        gq.load()
+        if dist.rank == 0:
+            run_sweep(load_peaks()[0])
+        dist.close()
+        return
     if args.impl == "reference":
         run_reference(args, dist)
         dist.close()
