@@ -149,6 +149,45 @@ constexpr int kQDsum = 2 * 4 * 128 * 4;                // bias-grad column sums 
 constexpr int kQSmem = 1024 + kQStages * kQTile + 2 * kQStageOut + 16 * 32 * 4 + 8 * 2 * kQStages + 16 +
                        kQScanBytes + kQDsum;
 
+// A CTA's walk over the tiles t = blockIdx.x + i * gridDim.x, in increasing
+// order: row tile rt, column tile ct, the group g that owns rt, and the ring
+// stage s with its phase, each advanced incrementally (no division and no
+// search per tile).  `g` stays valid while rt < s_tp[G], i.e. while tiles
+// remain.
+struct QTileWalk {
+    int64_t rt, step_rt;
+    int ct, step_ct, nct, g, s;
+    uint32_t ph;
+
+    __device__ __forceinline__ void init(const int32_t* s_tp, int G, int nct_)
+    {
+        nct = nct_;
+        rt = blockIdx.x / nct;
+        ct = (int)(blockIdx.x % nct);
+        step_rt = gridDim.x / nct;
+        step_ct = (int)(gridDim.x % nct);
+        g = rt < s_tp[G] ? group_of_tile(s_tp, G, rt) : G - 1;
+        s = 0;
+        ph = 0;
+    }
+
+    __device__ __forceinline__ void next(const int32_t* s_tp, int G)
+    {
+        rt += step_rt;
+        ct += step_ct;
+        if (ct >= nct) {
+            ct -= nct;
+            ++rt;
+        }
+        while (g < G - 1 && s_tp[g + 1] <= rt)
+            ++g;
+        if (++s == kQStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 // Output tensor maps of k_quant_mx: codes of one orientation as [rows, cols]
 // uint8 with 128-byte swizzle, boxes of 128 columns x 128 rows (whole tiles)
 // and 128 columns x 32 rows (the live part of a group's last tile).
@@ -207,14 +246,16 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
         if (lane == 0) {
             ptx::prefetch_tmap(&tma_x);
             int64_t it = 0;
-            for (int64_t t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++it) {
-                const int s = (int)(it % kQStages);
-                const uint32_t ph = (uint32_t)((it / kQStages) & 1);
+            QTileWalk wk;
+            wk.init(s_tp, G, nct);
+            for (int64_t t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++it, wk.next(s_tp, G)) {
+                const int s = wk.s;
+                const uint32_t ph = wk.ph;
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort, status))
                     break;
-                const int64_t rt = t / nct;
-                const int ct = (int)(t - rt * nct);
-                const int g = group_of_tile(s_tp, G, rt);
+                const int64_t rt = wk.rt;
+                const int ct = wk.ct;
+                const int g = wk.g;
                 const int32_t row0 = (int32_t)(s_off[g] + 128 * (rt - s_tp[g]));
                 ptx::mbar_arrive_expect_tx(&full[s], kQTile);
                 ptx::tma_load_2d(tiles + s * kQTile, &tma_x, &full[s], ct * 128, row0);
@@ -240,12 +281,14 @@ k_quant_mx(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ Qu
     const uint32_t r_in_tile = 32 * rb + lane;
     const bool lead = threadIdx.x == 0;
     int64_t it = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-        const int s = (int)(it % kQStages);
-        const uint32_t ph = (uint32_t)((it / kQStages) & 1);
-        const int64_t rt = t / nct;
-        const int ct = (int)(t - rt * nct);
-        const int g = group_of_tile(s_tp, G, rt);
+    QTileWalk wk;
+    wk.init(s_tp, G, nct);
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it, wk.next(s_tp, G)) {
+        const int s = wk.s;
+        const uint32_t ph = wk.ph;
+        const int64_t rt = wk.rt;
+        const int ct = wk.ct;
+        const int g = wk.g;
         const int64_t lt = rt - s_tp[g];
         const int64_t m = s_off[g + 1] - s_off[g];
         const int rows_here = (int)min((int64_t)128, m - 128 * lt);   // a multiple of 32
