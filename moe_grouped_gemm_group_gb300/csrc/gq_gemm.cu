@@ -623,6 +623,20 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         int ps = 0;                                       // stage of the next load, its phase
         uint32_t pph = 0;
         const bool front = (int)blockIdx.x < p.front_ctas;
+        // Run-time order: with accumulate, the empty groups (last in the
+        // size order) have nothing to do and stay out of the claims.  The
+        // next claim is issued while the current tile's loads go out, so its
+        // round trip is hidden.
+        int64_t nclaim = ntiles, claimed = -1;
+        if (dyn) {
+            if (p.accumulate) {
+                int live = 0;
+                for (int g = 0; g < p.G; ++g)
+                    live += c.s_off[g + 1] > c.s_off[g];
+                nclaim = (int64_t)live * (ntiles / p.G);
+            }
+            claimed = claim_tile(p.claim, front, nclaim);
+        }
         while (!*c.abort) {
             int64_t tile;
             if (!dyn) {
@@ -631,7 +645,9 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 if (tile >= ntiles)
                     break;
             } else {
-                tile = claim_tile(p.claim, front, ntiles);
+                tile = claimed;
+                if (tile >= 0)
+                    claimed = claim_tile(p.claim, front, nclaim);
                 if (tile >= 0 && decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord).skip)
                     continue;
                 if (!ring_put(ring_full, ring_empty, s_ring, rq, tile, c.abort, p.status) || tile < 0)
