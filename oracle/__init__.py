@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_SPLITS, ERR_UNSUPPORTED = 0, -1, -2, -3, -4
-RECIPE_MX, RECIPE_CHANNEL = 0, 1
+RECIPE_MX, RECIPE_CHANNEL, RECIPE_NVFP4 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -81,6 +81,19 @@ def _load():
             lib.or_srelu_quantize_mx.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                                  C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p,
                                                  C.c_void_p, C.c_int64]
+            lib.or_e2m1_decode.restype = C.c_double
+            lib.or_e2m1_decode.argtypes = [C.c_uint8]
+            lib.or_e2m1_encode.restype = C.c_uint8
+            lib.or_e2m1_encode.argtypes = [C.c_double]
+            lib.or_nv_global_scale.restype = C.c_float
+            lib.or_nv_global_scale.argtypes = [C.c_float]
+            lib.or_quantize_nvfp4.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int,
+                                              C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int64,
+                                              C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
+            lib.or_gemm_nvfp4.argtypes = ([C.c_int] + [C.c_void_p] * 7 +
+                                          [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int, C.c_void_p])
+            for name in ("or_quantize_nvfp4", "or_gemm_nvfp4"):
+                getattr(lib, name).restype = C.c_int
             for name in ("or_split_scan", "or_quantize_mx", "or_quantize_channel", "or_srelu_quantize_mx",
                          "or_gemm_fprop", "or_gemm_dgrad", "or_gemm_wgrad_mx",
                          "or_gemm_wgrad_channel", "or_gemm_sample", "or_grouped_bias_add",
@@ -236,6 +249,88 @@ def quantize_channel(x_bits, splits, num_groups: int, zero_scale: float = 1e-30,
                                  _p(cd), _p(cs), cs.size)
     _check(st, "quantize_channel")
     return ChannelQuantized(cd, cs[:L // 128], s, R, Cc)
+
+
+# --------------------------------------------------------------------------- #
+# NVFP4                                                                        #
+# --------------------------------------------------------------------------- #
+
+def e2m1_decode(code: int) -> float:
+    return float(_load().or_e2m1_decode(int(code)))
+
+
+def e2m1_encode(value: float) -> int:
+    return int(_load().or_e2m1_encode(float(value)))
+
+
+def nv_global_scale(amax: float) -> float:
+    """The second-level scale S_g of a group with this amax (fp32)."""
+    return float(_load().or_nv_global_scale(float(amax)))
+
+
+def scale_bytes_nvfp4(splits, num_groups, rows_cap, cols) -> int:
+    """Bytes of the grouped NVFP4 scale regions: 512 (cols/64) sum_g T_g."""
+    _, tp, _ = split_scan(splits, num_groups, rows_cap, cols)
+    return int(512 * (cols // 64) * tp[-1])
+
+
+class NVQuantized:
+    """Host copy of an NVFP4-quantised buffer: rowwise codes [R, C/2] and
+    transposed columnwise codes [C, R/2] (two E2M1 codes a byte), swizzled
+    E4M3 scale bytes per orientation, and the per-group amax (fp32 [G])."""
+
+    def __init__(self, row_data, row_scale, col_data, col_scale, amax, splits, rows_cap, cols):
+        self.row_data, self.row_scale = row_data, row_scale
+        self.col_data, self.col_scale = col_data, col_scale
+        self.amax = amax
+        self.splits, self.rows_cap, self.cols = splits, rows_cap, cols
+
+
+def quantize_nvfp4(x_bits, splits, num_groups: int, rowwise=True, colwise=True,
+                   data_fill: int = 0, scale_fill: int = 0) -> NVQuantized:
+    """NVFP4 quantisation of a bf16 [R, C] buffer (uint16 bits); code bytes of
+    rows past the live total keep ``data_fill``, scale bytes past the grouped
+    extent ``scale_fill``."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, Cc = x.shape
+    s = _splits(splits)
+    need = scale_bytes_nvfp4(s, num_groups, R, Cc)
+    rd = np.full((R, Cc // 2), data_fill, np.uint8) if rowwise else None
+    cd = np.full((Cc, R // 2), data_fill, np.uint8) if colwise else None
+    rs = np.full(max(need, 1), scale_fill, np.uint8) if rowwise else None
+    cs = np.full(max(need, 1), scale_fill, np.uint8) if colwise else None
+    amax = np.zeros(num_groups, np.float32)
+    st = lib.or_quantize_nvfp4(_p(x), R, Cc, _p(s), num_groups, int(rowwise), int(colwise),
+                               _p(rd), _p(rs), need, _p(cd), _p(cs), need, _p(amax))
+    _check(st, "quantize_nvfp4")
+    return NVQuantized(rd, rs, cd, cs, amax, s, R, Cc)
+
+
+def gemm_nvfp4(kind: str, a: NVQuantized, b: NVQuantized, splits, num_groups, N, K,
+               accumulate: bool = False, init: np.ndarray | None = None) -> np.ndarray:
+    """Grouped GEMMs on NVFP4 operands, fp64:
+    'fprop' Y = X_g W_g^T [R, N] (a = X rowwise, b = W rowwise);
+    'dgrad' dX = dY_g W_g [R, K] (a = dY rowwise, b = W columnwise);
+    'wgrad' dW[g] = (init[g] if accumulate) + dY_g^T X_g [G, N, K] (both columnwise).
+    Rows past the live total of Y / dX are NaN."""
+    lib = _load()
+    R = a.rows_cap
+    if kind == "fprop":
+        k, ad, as_, bd, bs, y = 0, a.row_data, a.row_scale, b.row_data, b.row_scale, np.full((R, N), np.nan)
+    elif kind == "dgrad":
+        k, ad, as_, bd, bs, y = 1, a.row_data, a.row_scale, b.col_data, b.col_scale, np.full((R, K), np.nan)
+    elif kind == "wgrad":
+        k, ad, as_, bd, bs = 2, a.col_data, a.col_scale, b.col_data, b.col_scale
+        y = (np.zeros((num_groups, N, K)) if init is None
+             else np.ascontiguousarray(init, dtype=np.float64).copy())
+    else:
+        raise ValueError(kind)
+    st = lib.or_gemm_nvfp4(k, _p(ad), _p(as_), _p(np.ascontiguousarray(a.amax, np.float32)), _p(bd), _p(bs),
+                           _p(np.ascontiguousarray(b.amax, np.float32)), _p(_splits(splits)), num_groups, R,
+                           N, K, int(accumulate), _p(y))
+    _check(st, "gemm_nvfp4")
+    return y
 
 
 # --------------------------------------------------------------------------- #

@@ -46,6 +46,7 @@
  *  - MX needs every split % 32 == 0, the per-channel recipe % 128 == 0, and
  *    cols % 128 == 0; anything else is rejected, not padded.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -776,5 +777,297 @@ int or_srelu_quantize_mx(const float* y, const float* probs, int64_t rows_cap, i
     }
     free(a);
     free(off);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4: E2M1 codes, 16-element blocks with E4M3 scales, and one fp32       */
+/* second-level scale per group                                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages name NVFP4 as a second quantiser on the same grouped code paths
+ * (TransformerEngine PR 3224, the NVFP4 note beside the MXFP8 changes)
+ * without defining it.  Reading taken: the public NVFP4 format.
+ *  - Codes are FP4 E2M1 (values +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}); conversion
+ *    rounds to nearest, ties to even, saturates to +-6, and a value that
+ *    rounds to zero keeps its sign.  Two codes per byte, the element with the
+ *    even index in the low nibble.
+ *  - Group g's second-level scale, fp32: S_g = 2688 / amax_g (2688 = 448 * 6,
+ *    the largest E4M3 scale times the largest E2M1 magnitude), S_g = 1 when
+ *    amax_g == 0, clamped to FLT_MAX; amax_g is the largest |x| over the
+ *    group's live rows.
+ *  - Each block of 16 consecutive elements along the contraction axis, in
+ *    fp32 op by op: s = (amax_b / 6) * S_g; its E4M3 byte sf = e4m3(s)
+ *    (nearest-even, saturating); m = S_g / sf (0 when sf == 0, clamped to
+ *    FLT_MAX); codes = e2m1(x * m).  The value a code stands for is
+ *    e2m1(code) * sf / S_g.
+ *  - Rowwise codes [rows_cap, cols/2] (blocks along a row); columnwise codes
+ *    are stored transposed, [cols, rows_cap/2] (blocks of 16 rows, the
+ *    column's codes contiguous), so that every GEMM operand is K-major.
+ *  - Scale bytes use the 512-byte [32][4][4] atom of the MX layout with 16
+ *    elements per scale, so an atom covers 128 rows (channels) x 64
+ *    elements.  Group g's region starts at byte 512 * (cols/64) * (T_0 + ...
+ *    + T_{g-1}), T_h = ceil(m_h / 128), for both orientations.  Rowwise
+ *    atoms are ordered [128-row tile][64-column block]; columnwise atoms
+ *    [128-column tile][64-row block], the group's 2 T_g row blocks the inner
+ *    stride.  Entries that cover no live row are 0.
+ */
+static const double e2m1_magnitudes[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Value of an E2M1 nibble: sign bit 3, then the magnitude index 0..7. */
+double or_e2m1_decode(uint8_t code)
+{
+    double v = e2m1_magnitudes[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+/* Nearest E2M1 code to v (ties to the even magnitude index), saturating. */
+uint8_t or_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs(v), quantum, q, n, r;
+    if (isnan(v))
+        return 7;
+    if (a >= 6.0)
+        return sign | 7;
+    /* spacing of the codes around a: 0.5 below 2, 1 in [2, 4), 2 in [4, 6] */
+    quantum = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    q = a / quantum;                 /* exact: quantum is a power of two */
+    n = floor(q);
+    if (q - n > 0.5 || (q - n == 0.5 && fmod(n, 2.0) != 0.0))
+        n += 1.0;
+    r = n * quantum;
+    for (int c = 0; c < 8; ++c)
+        if (e2m1_magnitudes[c] == r)
+            return sign | (uint8_t)c;
+    return sign | 7;
+}
+
+/* Second-level scale S_g of a group from its amax. */
+float or_nv_global_scale(float amax)
+{
+    volatile float s;
+    if (amax == 0.0f)
+        return 1.0f;
+    s = 2688.0f / amax;
+    return s > FLT_MAX ? FLT_MAX : s;
+}
+
+/* One block of 16 elements x[0], x[stride], ...: its scale byte, and codes. */
+static uint8_t nv_block(const uint16_t* x, int64_t stride, float S, uint8_t* codes)
+{
+    float amax = 0.0f, m = 0.0f;
+    volatile float s;
+    uint8_t sf;
+    for (int i = 0; i < 16; ++i) {
+        float a = fabsf(bf16_value_f32(x[i * stride]));
+        if (a > amax)
+            amax = a;
+    }
+    s = amax / 6.0f;
+    s = s * S;
+    sf = or_e4m3_encode((double)s);
+    if (sf != 0) {
+        volatile float mm = S / (float)or_e4m3_decode(sf);
+        m = mm > FLT_MAX ? FLT_MAX : mm;
+    }
+    for (int i = 0; i < 16; ++i) {
+        volatile float q = bf16_value_f32(x[i * stride]) * m;     /* one fp32 rounding */
+        codes[i] = or_e2m1_encode((double)q);
+    }
+    return sf;
+}
+
+static void put_nibble(uint8_t* base, int64_t i, uint8_t code)
+{
+    if (i % 2 == 0)
+        base[i / 2] = (uint8_t)((base[i / 2] & 0xF0) | (code & 0x0F));
+    else
+        base[i / 2] = (uint8_t)((base[i / 2] & 0x0F) | (uint8_t)(code << 4));
+}
+
+static uint8_t get_nibble(const uint8_t* base, int64_t i)
+{
+    return (uint8_t)((i % 2 == 0) ? (base[i / 2] & 0x0F) : (base[i / 2] >> 4));
+}
+
+/* Byte offset of group g's NVFP4 scale region for a buffer of `cols` columns. */
+static int64_t nv_region(int64_t cols, int64_t tile_prefix) { return 512 * (cols / 64) * tile_prefix; }
+
+int or_quantize_nvfp4(const uint16_t* x, int64_t rows_cap, int64_t cols, const int32_t* splits, int G,
+                      int rowwise, int colwise, uint8_t* row_data, uint8_t* row_scale, int64_t row_scale_bytes,
+                      uint8_t* col_data, uint8_t* col_scale, int64_t col_scale_bytes, float* amax_out)
+{
+    int64_t *off = malloc(sizeof(int64_t) * (G + 1) * 3);
+    int64_t *tp, end;
+    int st;
+    if (!off)
+        return OR_ERR_INVALID_ARG;
+    tp = off + (G + 1);
+    st = or_split_scan(splits, G, rows_cap, cols, OR_RECIPE_MX, off, tp, off + 2 * (G + 1));
+    if (st != OR_OK || (!rowwise && !colwise)) {
+        free(off);
+        return st != OR_OK ? st : OR_ERR_INVALID_ARG;
+    }
+    end = nv_region(cols, tp[G]);
+    if ((rowwise && end > row_scale_bytes) || (colwise && end > col_scale_bytes)) {
+        free(off);
+        return OR_ERR_INVALID_ARG;
+    }
+    if (colwise && rows_cap % 2 != 0) {
+        free(off);
+        return OR_ERR_ALIGNMENT;
+    }
+    if (rowwise)
+        memset(row_scale, 0, (size_t)end);
+    if (colwise)
+        memset(col_scale, 0, (size_t)end);
+
+    for (int g = 0; g < G; ++g) {
+        int64_t o = off[g], m = off[g + 1] - off[g], T = tp[g + 1] - tp[g];
+        int64_t sb = nv_region(cols, tp[g]);
+        float amax = 0.0f, S;
+        for (int64_t r = o; r < o + m; ++r)
+            for (int64_t c = 0; c < cols; ++c) {
+                float a = fabsf(bf16_value_f32(x[r * cols + c]));
+                if (a > amax)
+                    amax = a;
+            }
+        amax_out[g] = amax;
+        S = or_nv_global_scale(amax);
+        if (rowwise) {
+#pragma omp parallel for schedule(static)
+            for (int64_t lr = 0; lr < m; ++lr) {
+                int64_t r = o + lr;
+                uint8_t codes[16];
+                for (int64_t j = 0; j < cols / 16; ++j) {
+                    uint8_t sf = nv_block(x + r * cols + 16 * j, 1, S, codes);
+                    for (int i = 0; i < 16; ++i)
+                        put_nibble(row_data + r * (cols / 2), 16 * j + i, codes[i]);
+                    row_scale[sb + ((lr / 128) * (cols / 64) + j / 4) * 512 + atom_byte(lr % 128, j % 4)] = sf;
+                }
+            }
+        }
+        if (colwise) {
+#pragma omp parallel for schedule(static)
+            for (int64_t c = 0; c < cols; ++c) {
+                uint8_t codes[16];
+                for (int64_t b = 0; b < m / 16; ++b) {
+                    uint8_t sf = nv_block(x + (o + 16 * b) * cols + c, cols, S, codes);
+                    for (int i = 0; i < 16; ++i)
+                        put_nibble(col_data + c * (rows_cap / 2), o + 16 * b + i, codes[i]);
+                    col_scale[sb + ((c / 128) * 2 * T + b / 4) * 512 + atom_byte(c % 128, b % 4)] = sf;
+                }
+            }
+        }
+    }
+    free(off);
+    return OR_OK;
+}
+
+/* NVFP4 element (r, c) of the [rows, cols] operand (group g), from rowwise
+ * or transposed columnwise storage. */
+static double nv_elem(const layout_t* l, int64_t rows_cap, const uint8_t* data, const uint8_t* scale,
+                      const float* amax, int colwise, int g, int64_t r, int64_t c)
+{
+    int64_t lr = r - l->off[g], T = l->tp[g + 1] - l->tp[g];
+    int64_t sb = nv_region(l->cols, l->tp[g]);
+    uint8_t code, sf;
+    if (!colwise) {
+        int64_t j = c / 16;
+        code = get_nibble(data + r * (l->cols / 2), c);
+        sf = scale[sb + ((lr / 128) * (l->cols / 64) + j / 4) * 512 + atom_byte(lr % 128, j % 4)];
+    } else {
+        int64_t b = lr / 16;
+        code = get_nibble(data + c * (rows_cap / 2), r);
+        sf = scale[sb + ((c / 128) * 2 * T + b / 4) * 512 + atom_byte(c % 128, b % 4)];
+    }
+    return or_e2m1_decode(code) * or_e4m3_decode(sf) / (double)or_nv_global_scale(amax[g]);
+}
+
+/* Rows [0, L) of an NVFP4 operand as a dense fp64 [L, cols] array. */
+static double* deq_nv(const layout_t* l, int64_t rows_cap, const uint8_t* data, const uint8_t* scale,
+                      const float* amax, int colwise)
+{
+    int64_t L = l->off[l->G];
+    double* out = malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)l->cols);
+    if (!out)
+        return NULL;
+    for (int g = 0; g < l->G; ++g) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = l->off[g]; r < l->off[g + 1]; ++r)
+            for (int64_t c = 0; c < l->cols; ++c)
+                out[r * l->cols + c] = nv_elem(l, rows_cap, data, scale, amax, colwise, g, r, c);
+    }
+    return out;
+}
+
+/* Grouped GEMMs on NVFP4 operands, fp64 on the dequantised values:
+ *  kind 0 fprop: a = X rowwise [rows_cap, K], b = W rowwise [G*N, K];
+ *                y[o_g + r, n] = sum_k X[o_g + r, k] W_g[n, k]
+ *  kind 1 dgrad: a = dY rowwise [rows_cap, N], b = W columnwise (stored [K, G*N/2]);
+ *                y[o_g + r, k] = sum_n dY[o_g + r, n] W_g[n, k]
+ *  kind 2 wgrad: a = dY columnwise (stored [N, rows_cap/2]), b = X columnwise
+ *                (stored [K, rows_cap/2]); y[g, n, k] = (accumulate ? y : 0)
+ *                + sum over the live rows r of group g of dY[o_g + r, n] X[o_g + r, k]
+ * a_amax / b_amax: the operands' per-group amax (weights: one per expert). */
+int or_gemm_nvfp4(int kind, const uint8_t* a_data, const uint8_t* a_scale, const float* a_amax,
+                  const uint8_t* b_data, const uint8_t* b_scale, const float* b_amax, const int32_t* splits,
+                  int G, int64_t rows_cap, int64_t N, int64_t K, int accumulate, double* y)
+{
+    scan_t sa, sb;
+    double *A, *B;
+    int64_t wrows = (int64_t)G * N;
+    int st;
+    if (kind < 0 || kind > 2)
+        return OR_ERR_INVALID_ARG;
+    st = make_layout(&sa, splits, G, rows_cap, kind == 0 ? K : N, OR_RECIPE_MX);
+    if (st != OR_OK)
+        return st;
+    if (kind == 2)
+        st = make_layout(&sb, splits, G, rows_cap, K, OR_RECIPE_MX);
+    else
+        st = make_layout(&sb, NULL, G, wrows, K, OR_RECIPE_MX);
+    if (st != OR_OK) {
+        free(sa.buf);
+        return st;
+    }
+    A = deq_nv(&sa.l, rows_cap, a_data, a_scale, a_amax, kind == 2);
+    B = deq_nv(&sb.l, kind == 2 ? rows_cap : wrows, b_data, b_scale, b_amax, kind != 0);
+    for (int g = 0; g < G; ++g) {
+        int64_t o = sa.l.off[g], m = sa.l.off[g + 1] - o;
+        if (kind == 0) {
+#pragma omp parallel for schedule(static)
+            for (int64_t r = o; r < o + m; ++r)
+                for (int64_t n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < K; ++k)
+                        acc += A[r * K + k] * B[((int64_t)g * N + n) * K + k];
+                    y[r * N + n] = acc;
+                }
+        } else if (kind == 1) {
+#pragma omp parallel for schedule(static)
+            for (int64_t r = o; r < o + m; ++r)
+                for (int64_t k = 0; k < K; ++k) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n)
+                        acc += A[r * N + n] * B[((int64_t)g * N + n) * K + k];
+                    y[r * K + k] = acc;
+                }
+        } else {
+#pragma omp parallel for schedule(static)
+            for (int64_t n = 0; n < N; ++n)
+                for (int64_t k = 0; k < K; ++k) {
+                    double acc = 0.0;
+                    for (int64_t r = o; r < o + m; ++r)
+                        acc += A[r * N + n] * B[r * K + k];
+                    y[((int64_t)g * N + n) * K + k] = accumulate ? y[((int64_t)g * N + n) * K + k] + acc : acc;
+                }
+        }
+    }
+    free(A);
+    free(B);
+    free(sa.buf);
+    free(sb.buf);
     return OR_OK;
 }
