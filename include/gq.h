@@ -75,7 +75,18 @@ typedef enum gq_recipe_kind {
     /* Per-channel 128-row fp32 scale (columnwise only), computed op by op in
      * fp32: sf = amax / 448; sf == 0 -> zero_scale; sf = max(sf, 1e-30);
      * codes = e4m3(x * (1 / sf)). */
-    GQ_RECIPE_CHANNEL128_F32 = 1
+    GQ_RECIPE_CHANNEL128_F32 = 1,
+    /* NVFP4: FP4 E2M1 codes with one E4M3 scale per 16 elements along the
+     * contraction axis and one fp32 second-level scale per group.  The pages
+     * name NVFP4 beside MXFP8 on the grouped paths (TransformerEngine PR
+     * 3224) without defining it; this is the public NVFP4 format.  Per group
+     * g: amax_g = max |x| over its live rows, S_g = 2688 / amax_g (1 when
+     * amax_g == 0, clamped to FLT_MAX).  Per block, in fp32 op by op:
+     * s = (amax_b / 6) * S_g, sf = e4m3(s) (nearest-even, saturating),
+     * m = S_g / sf (0 when sf == 0, clamped to FLT_MAX), codes =
+     * e2m1(x * m) (nearest-even, saturating to +-6).  A code stands for
+     * e2m1 * sf / S_g. */
+    GQ_RECIPE_NVFP4_1X16 = 2
 } gq_recipe_kind;
 
 typedef enum gq_dtype { GQ_DTYPE_F32 = 0, GQ_DTYPE_BF16 = 1 } gq_dtype;
@@ -107,6 +118,21 @@ typedef struct gq_recipe {
  *      Entries of a group's last tile that cover no live row are 0.
  *  col_scale (per-channel) : fp32 [L/128][cols]: the scale of live rows
  *      [128 b, 128 b + 128) of channel c is element b * cols + c.
+ *  NVFP4 : two E2M1 codes a byte, the element with the even index in the low
+ *      nibble.  row_data is [rows_cap, cols/2]; col_data is stored
+ *      TRANSPOSED, [cols, rows_cap/2] (row c holds column c's codes in blocks
+ *      of 16 rows), so that every GEMM operand has its contraction axis
+ *      contiguous (the tensor core takes packed 4-bit operands K-major only);
+ *      columnwise quantisation needs rows_cap % 32 == 0.  Scale bytes (E4M3)
+ *      use the same 512-byte atom with 16 elements a scale, so an atom
+ *      covers 128 rows (channels) x 64 elements; group g's region starts at
+ *      512 * (cols/64) * (T_0 + ... + T_{g-1}) in both orientations; rowwise
+ *      atoms are ordered [128-row tile][64-column block], columnwise atoms
+ *      [128-column tile][64-row block] (2 T_g inner).  Byte of (row r,
+ *      16-column block j) -- columnwise (channel r, 16-row block j) -- inside
+ *      an atom: (r % 32) * 16 + (r / 32) * 4 + j % 4.
+ *  amax (NVFP4 only) : device fp32 [num_groups], the per-group amax the
+ *      quantiser wrote (4-byte aligned); the GEMMs read it to undo S_g.
  *  *_scale_bytes : capacity in bytes of each scale buffer (checked).
  *
  * Device buffers must be 16-byte aligned.
@@ -123,6 +149,7 @@ typedef struct gq_quantized {
     void* col_scale;
     uint64_t row_scale_bytes;
     uint64_t col_scale_bytes;
+    float* amax;
 } gq_quantized;
 
 /* Human-readable name of a status code (static storage). */
@@ -133,7 +160,8 @@ int32_t gq_version(void);
 
 /* Bytes a scale buffer needs for any split table of num_groups groups over
  * rows_cap rows: MX 512 * (cols/128) * (ceil(rows_cap/128) + num_groups);
- * per-channel 4 * cols * (rows_cap / 128).  0 on a bad argument. */
+ * NVFP4 512 * (cols/64) * (ceil(rows_cap/128) + num_groups); per-channel
+ * 4 * cols * (rows_cap / 128).  0 on a bad argument. */
 uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64_t rows_cap,
                               int64_t cols);
 
@@ -165,6 +193,8 @@ gq_status gq_split_scan(const int32_t* d_split_sizes, int32_t num_groups, int64_
  *   overwritten with *recipe.
  * Reads rows < L of x only; writes codes of rows < L and the grouped scale
  * regions (bytes past the last group's region are untouched).
+ * NVFP4 runs three kernels: the split scan with amax[g] = 0, the per-group
+ * amax over the live rows, then the codes and scales; out->amax must be set.
  */
 gq_status gq_quantize(const void* x_bf16, int64_t rows_cap, int64_t cols,
                       const int32_t* d_split_sizes, int32_t num_groups, const gq_recipe* recipe,
@@ -203,6 +233,10 @@ gq_status gq_quantize_dbias(const void* x_bf16, int64_t rows_cap, int64_t cols,
  *   y : [R, n] of out_dtype (GQ_DTYPE_F32 or GQ_DTYPE_BF16, nearest-even);
  *       rows < L written, rows >= L untouched.
  * n and k must be multiples of 128.
+ * NVFP4 operands (x and w both NVFP4 rowwise): n and k must be multiples of
+ * 256; the fp32 accumulator of the block-scaled MMAs is multiplied by
+ * 1 / (S_x,g S_w,g) before the conversion.  Bias and the fused activation
+ * take MX operands only.
  */
 gq_status gq_gemm_fprop(const gq_quantized* x, const gq_quantized* w,
                         const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
@@ -259,6 +293,8 @@ gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w
  *   w  : MX columnwise (32-row blocks along n, group-local layout), rows_cap
  *        num_groups * n, cols k.
  *   dx : [R, k] of out_dtype; rows < L written.
+ * NVFP4: dy NVFP4 rowwise and w NVFP4 columnwise (stored [k, G n/2]); n and
+ * k multiples of 256.
  */
 gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
                         const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
@@ -269,7 +305,10 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
  *   dW_g = (accumulate ? dW_g : 0) + dY_g^T X_g
  * contracting over group g's live rows only (TransformerEngine issue 3484;
  * DeepGEMM issue 365, k_grouped_fp8_gemm_nt_contiguous with recipe (1,1,128)).
- *   dy, x : both MX columnwise, or both per-channel; rows_cap R; cols n and k.
+ *   dy, x : both MX columnwise, both NVFP4 columnwise (k a multiple of 256;
+ *           a group's last 64-row block may be half live: the scales of its
+ *           dead 16-row blocks are 0), or both per-channel; rows_cap R; cols
+ *           n and k.
  *   dw    : fp32 [num_groups, n, k].  accumulate = 1 adds into it (the
  *           accumulate_into_main_grad of TransformerEngine issue 3484); an
  *           empty group then leaves dW_g bit-unchanged, with accumulate = 0
@@ -285,7 +324,7 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
  *           (with skewed splits every CTA would otherwise work through the
  *           same group at the same time).  NULL keeps a static round-robin
  *           order.  Two calls that may run at the same time must not share a
- *           workspace.  The per-channel recipe ignores it.
+ *           workspace.  The per-channel and NVFP4 recipes ignore it.
  *   workspace_bytes : size of d_workspace (ignored when it is NULL).
  * Deterministic: every output element is produced by one CTA in a fixed
  * order of additions, whichever CTA that is; repeated calls, with or without

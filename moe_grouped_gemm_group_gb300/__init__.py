@@ -18,13 +18,13 @@ __all__ = [
     "gq_status_string", "gq_version", "gq_scale_bytes_bound", "gq_split_scan", "gq_quantize",
     "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_gemm_wgrad_noalloc", "alloc_quantized",
     "gq_gemm_fprop_bias", "gq_quantize_dbias", "gq_dbias_workspace_bytes", "gq_gemm_fprop_srelu_quant",
-    "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "DTYPE_F32", "DTYPE_BF16", "STATUS",
+    "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "RECIPE_NVFP4_1X16", "DTYPE_F32", "DTYPE_BF16", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libgq.so")
 
-RECIPE_MXFP8_1X32, RECIPE_CHANNEL128_F32 = 0, 1
+RECIPE_MXFP8_1X32, RECIPE_CHANNEL128_F32, RECIPE_NVFP4_1X16 = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 STATUS = {0: "GQ_OK", -1: "GQ_ERR_INVALID_ARG", -2: "GQ_ERR_ALIGNMENT", -3: "GQ_ERR_SPLITS",
           -4: "GQ_ERR_UNSUPPORTED", -5: "GQ_ERR_CUDA", -6: "GQ_ERR_TIMEOUT",
@@ -41,7 +41,7 @@ class Quantized(C.Structure):
     _fields_ = [("num_groups", C.c_int32), ("reserved0", C.c_int32), ("rows_cap", C.c_int64),
                 ("cols", C.c_int64), ("recipe", Recipe), ("row_data", C.c_void_p),
                 ("row_scale", C.c_void_p), ("col_data", C.c_void_p), ("col_scale", C.c_void_p),
-                ("row_scale_bytes", C.c_uint64), ("col_scale_bytes", C.c_uint64)]
+                ("row_scale_bytes", C.c_uint64), ("col_scale_bytes", C.c_uint64), ("amax", C.c_void_p)]
 
 
 class GQError(RuntimeError):
@@ -136,14 +136,15 @@ class GroupedTensor:
     ``gq_quantized`` descriptor, kept alive together with it."""
 
     def __init__(self, num_groups, rows_cap, cols, recipe: Recipe, row_data=None, row_scale=None,
-                 col_data=None, col_scale=None):
+                 col_data=None, col_scale=None, amax=None):
         self.row_data, self.row_scale = row_data, row_scale
         self.col_data, self.col_scale = col_data, col_scale
+        self.amax = amax
         self.desc = Quantized()
         d = self.desc
         d.num_groups, d.rows_cap, d.cols = num_groups, rows_cap, cols
         d.recipe = Recipe(recipe.kind, recipe.rowwise, recipe.colwise, recipe.zero_scale)
-        for name in ("row_data", "row_scale", "col_data", "col_scale"):
+        for name in ("row_data", "row_scale", "col_data", "col_scale", "amax"):
             t = getattr(self, name)
             setattr(d, name, None if t is None else _ptr(t, name).value)
         d.row_scale_bytes = 0 if row_scale is None else row_scale.numel() * row_scale.element_size()
@@ -166,6 +167,8 @@ def alloc_quantized(rows_cap: int, cols: int, num_groups: int, recipe: Recipe, d
                     fill: int | None = None) -> GroupedTensor:
     """Allocate (with torch) the buffers of a grouped quantised tensor.
 
+    NVFP4 codes take half a byte: rowwise [rows_cap, cols/2], columnwise
+    stored transposed [cols, rows_cap/2], plus the fp32 [num_groups] amax.
     ``fill`` optionally pre-fills every byte (a canary for tests)."""
     import torch
     nbytes = gq_scale_bytes_bound(recipe, num_groups, rows_cap, cols)
@@ -173,7 +176,12 @@ def alloc_quantized(rows_cap: int, cols: int, num_groups: int, recipe: Recipe, d
         raise ValueError("bad recipe or shape for gq_scale_bytes_bound")
     mk = torch.empty if fill is None else (lambda *a, **k: torch.full(*a, fill, **k))
 
-    def data():
+    nv = recipe.kind == RECIPE_NVFP4_1X16
+
+    def data(colwise=False):
+        if nv:
+            shape = (cols, rows_cap // 2) if colwise else (rows_cap, cols // 2)
+            return mk(shape, dtype=torch.uint8, device=device)
         return mk((rows_cap, cols), dtype=torch.uint8, device=device)
 
     def scale():
@@ -186,9 +194,14 @@ def alloc_quantized(rows_cap: int, cols: int, num_groups: int, recipe: Recipe, d
 
     rd = data() if recipe.rowwise else None
     rs = scale() if recipe.rowwise else None
-    cd = data() if recipe.colwise else None
+    cd = data(True) if recipe.colwise else None
     cs = scale() if recipe.colwise else None
-    return GroupedTensor(num_groups, rows_cap, cols, recipe, rd, rs, cd, cs)
+    am = None
+    if nv:
+        am = torch.empty((max(num_groups, 4),), dtype=torch.float32, device=device)
+        if fill is not None:
+            am.view(torch.uint8).fill_(fill)
+    return GroupedTensor(num_groups, rows_cap, cols, recipe, rd, rs, cd, cs, am)
 
 
 # --------------------------------------------------------------------------- #

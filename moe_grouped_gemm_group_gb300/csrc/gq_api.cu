@@ -20,6 +20,13 @@ uint64_t mx_scale_bound(int32_t G, int64_t rows_cap, int64_t cols)
     return 512ull * (uint64_t)(cols / 128) * (uint64_t)((rows_cap + 127) / 128 + G);
 }
 
+uint64_t nv_scale_bound(int32_t G, int64_t rows_cap, int64_t cols)
+{
+    return 512ull * (uint64_t)(cols / 64) * (uint64_t)((rows_cap + 127) / 128 + G);
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 uint64_t channel_scale_bound(int64_t rows_cap, int64_t cols)
 {
     return 4ull * (uint64_t)cols * (uint64_t)(rows_cap / 128);
@@ -90,6 +97,41 @@ gq_status quantize_impl(const void* x_bf16, int64_t rows_cap, int64_t cols,
             recipe->colwise ? (uint8_t*)out->col_data : nullptr, (uint8_t*)out->col_scale,
             d_status, (cudaStream_t)stream, dpart));
     }
+    if (recipe->kind == GQ_RECIPE_NVFP4_1X16) {
+        if (!recipe->rowwise && !recipe->colwise)
+            return GQ_ERR_INVALID_ARG;
+        const uint64_t need = nv_scale_bound(num_groups, rows_cap, cols);
+        if (!out->amax)
+            return GQ_ERR_INVALID_ARG;
+        if (!aligned4(out->amax))
+            return GQ_ERR_ALIGNMENT;
+        if (recipe->rowwise) {
+            if (live && (!out->row_data || !out->row_scale))
+                return GQ_ERR_INVALID_ARG;
+            if (live && (!aligned16(out->row_data) || !aligned16(out->row_scale)))
+                return GQ_ERR_ALIGNMENT;
+            if (out->row_scale_bytes < need)
+                return GQ_ERR_INVALID_ARG;
+        }
+        if (recipe->colwise) {
+            if (rows_cap % 32 != 0)
+                return GQ_ERR_ALIGNMENT;
+            if (live && (!out->col_data || !out->col_scale))
+                return GQ_ERR_INVALID_ARG;
+            if (live && (!aligned16(out->col_data) || !aligned16(out->col_scale)))
+                return GQ_ERR_ALIGNMENT;
+            if (out->col_scale_bytes < need)
+                return GQ_ERR_INVALID_ARG;
+        }
+        out->recipe = *recipe;
+        if (!live)
+            return GQ_OK;
+        return cuda_status(gq::launch_quant_nv(
+            x_bf16, rows_cap, cols, d_split_sizes, num_groups,
+            recipe->rowwise ? (uint8_t*)out->row_data : nullptr, (uint8_t*)out->row_scale,
+            recipe->colwise ? (uint8_t*)out->col_data : nullptr, (uint8_t*)out->col_scale, out->amax, d_status,
+            (cudaStream_t)stream));
+    }
     if (recipe->kind == GQ_RECIPE_CHANNEL128_F32) {
         if (recipe->rowwise || !recipe->colwise)
             return GQ_ERR_UNSUPPORTED;
@@ -128,7 +170,7 @@ const char* gq_status_string(int32_t status)
     }
 }
 
-int32_t gq_version(void) { return (1 << 16) | 0; }
+int32_t gq_version(void) { return (1 << 16) | 1; }
 
 uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64_t rows_cap,
                               int64_t cols)
@@ -139,6 +181,8 @@ uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64
         return mx_scale_bound(num_groups, rows_cap, cols);
     if (recipe->kind == GQ_RECIPE_CHANNEL128_F32)
         return channel_scale_bound(rows_cap, cols);
+    if (recipe->kind == GQ_RECIPE_NVFP4_1X16)
+        return nv_scale_bound(num_groups, rows_cap, cols);
     return 0;
 }
 
@@ -220,11 +264,33 @@ gq_status check_operand(const gq_quantized* q, int32_t kind, bool colwise, int32
     if (rows > 0 && (!aligned16(d) || !aligned16(s)))
         return GQ_ERR_ALIGNMENT;
     const uint64_t cap = colwise ? q->col_scale_bytes : q->row_scale_bytes;
-    const uint64_t need = kind == GQ_RECIPE_MXFP8_1X32 ? mx_scale_bound(G, rows, cols)
-                                                       : channel_scale_bound(rows, cols);
+    const uint64_t need = kind == GQ_RECIPE_MXFP8_1X32   ? mx_scale_bound(G, rows, cols)
+                          : kind == GQ_RECIPE_NVFP4_1X16 ? nv_scale_bound(G, rows, cols)
+                                                         : channel_scale_bound(rows, cols);
     if (cap < need)
         return GQ_ERR_INVALID_ARG;
+    if (kind == GQ_RECIPE_NVFP4_1X16) {
+        if (!q->amax)
+            return GQ_ERR_INVALID_ARG;
+        if (!aligned4(q->amax))
+            return GQ_ERR_ALIGNMENT;
+        if (colwise && rows % 32 != 0)
+            return GQ_ERR_ALIGNMENT;
+    }
     return GQ_OK;
+}
+
+// An NVFP4 operand as the GEMM reads it: rowwise [rows, cols/2], or
+// columnwise stored transposed [cols, rows/2].
+gq::NvOperand nv_operand(const gq_quantized* q, bool colwise)
+{
+    gq::NvOperand o;
+    o.data = (const uint8_t*)(colwise ? q->col_data : q->row_data);
+    o.scale = (const uint8_t*)(colwise ? q->col_scale : q->row_scale);
+    o.amax = q->amax;
+    o.rows = colwise ? q->cols : q->rows_cap;
+    o.row_bytes = colwise ? q->rows_cap / 2 : q->cols / 2;
+    return o;
 }
 
 gq::GemmOperand operand(const gq_quantized* q, bool colwise)
@@ -271,6 +337,19 @@ gq_status fprop_impl(const gq_quantized* x, const gq_quantized* w, const int32_t
         return st;
     if (out_dtype != GQ_DTYPE_F32 && out_dtype != GQ_DTYPE_BF16)
         return GQ_ERR_UNSUPPORTED;
+    if (x->recipe.kind == GQ_RECIPE_NVFP4_1X16) {
+        if (d_bias || act || n % 256 != 0 || k % 256 != 0)
+            return GQ_ERR_UNSUPPORTED;
+        if ((st = check_operand(x, GQ_RECIPE_NVFP4_1X16, false, num_groups, x->rows_cap, k)) != GQ_OK)
+            return st;
+        if ((st = check_operand(w, GQ_RECIPE_NVFP4_1X16, false, num_groups, (int64_t)num_groups * n, k)) !=
+            GQ_OK)
+            return st;
+        if (x->rows_cap == 0)
+            return GQ_OK;
+        return gq::launch_gemm_nv(gq::NV_FPROP, nv_operand(x, false), nv_operand(w, false), d_split_sizes,
+                                  num_groups, x->rows_cap, n, k, y, out_dtype, 0, d_status, (cudaStream_t)stream);
+    }
     if ((st = check_operand(x, GQ_RECIPE_MXFP8_1X32, false, num_groups, x->rows_cap, k)) != GQ_OK)
         return st;
     if ((st = check_operand(w, GQ_RECIPE_MXFP8_1X32, false, num_groups, (int64_t)num_groups * n,
@@ -355,6 +434,18 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
         return st;
     if (out_dtype != GQ_DTYPE_F32 && out_dtype != GQ_DTYPE_BF16)
         return GQ_ERR_UNSUPPORTED;
+    if (dy->recipe.kind == GQ_RECIPE_NVFP4_1X16) {
+        if (n % 256 != 0 || k % 256 != 0)
+            return GQ_ERR_UNSUPPORTED;
+        if ((st = check_operand(dy, GQ_RECIPE_NVFP4_1X16, false, num_groups, dy->rows_cap, n)) != GQ_OK)
+            return st;
+        if ((st = check_operand(w, GQ_RECIPE_NVFP4_1X16, true, num_groups, (int64_t)num_groups * n, k)) != GQ_OK)
+            return st;
+        if (dy->rows_cap == 0)
+            return GQ_OK;
+        return gq::launch_gemm_nv(gq::NV_DGRAD, nv_operand(dy, false), nv_operand(w, true), d_split_sizes,
+                                  num_groups, dy->rows_cap, n, k, dx, out_dtype, 0, d_status, (cudaStream_t)stream);
+    }
     if ((st = check_operand(dy, GQ_RECIPE_MXFP8_1X32, false, num_groups, dy->rows_cap, n)) != GQ_OK)
         return st;
     if ((st = check_operand(w, GQ_RECIPE_MXFP8_1X32, true, num_groups, (int64_t)num_groups * n,
@@ -386,7 +477,7 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
     if (dy->recipe.kind != x->recipe.kind)
         return GQ_ERR_UNSUPPORTED;
     const int32_t kind = dy->recipe.kind;
-    if (kind != GQ_RECIPE_MXFP8_1X32 && kind != GQ_RECIPE_CHANNEL128_F32)
+    if (kind != GQ_RECIPE_MXFP8_1X32 && kind != GQ_RECIPE_CHANNEL128_F32 && kind != GQ_RECIPE_NVFP4_1X16)
         return GQ_ERR_UNSUPPORTED;
     if (x->rows_cap != dy->rows_cap)
         return GQ_ERR_SHAPE_MISMATCH;
@@ -394,6 +485,13 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
         return st;
     if ((st = check_operand(x, kind, true, num_groups, x->rows_cap, k)) != GQ_OK)
         return st;
+    if (kind == GQ_RECIPE_NVFP4_1X16) {
+        if (k % 256 != 0)
+            return GQ_ERR_UNSUPPORTED;
+        return gq::launch_gemm_nv(gq::NV_WGRAD, nv_operand(dy, true), nv_operand(x, true), d_split_sizes,
+                                  num_groups, dy->rows_cap, n, k, dw, GQ_DTYPE_F32, accumulate, d_status,
+                                  (cudaStream_t)stream);
+    }
     return gq::launch_gemm(kind == GQ_RECIPE_MXFP8_1X32 ? gq::GEMM_WGRAD_MX
                                                         : gq::GEMM_WGRAD_CHANNEL,
                            operand(dy, true), operand(x, true), d_split_sizes, num_groups,

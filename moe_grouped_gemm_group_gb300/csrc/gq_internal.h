@@ -93,4 +93,22 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       cudaStream_t stream, void* workspace = nullptr, const void* bias = nullptr,
                       int bias_dtype = 0, const ActOutput* act = nullptr);
 
+// NVFP4 quantiser and GEMMs (gq_nvfp4.cu).  Operand buffers are already
+// validated; the quantiser runs the split scan + amax reset, the per-group
+// amax pass and the quantisation pass on `stream`.
+cudaError_t launch_quant_nv(const void* x, int64_t rows_cap, int64_t cols, const int32_t* splits, int G,
+                            uint8_t* row_data, uint8_t* row_scale, uint8_t* col_data, uint8_t* col_scale, float* amax,
+                            int32_t* status, cudaStream_t stream);
+struct NvOperand {
+    const uint8_t* data;   // packed E2M1 codes, [rows, row_bytes]
+    const uint8_t* scale;  // swizzled E4M3 scale atoms
+    const float* amax;     // per-group amax, fp32 [G]
+    int64_t rows;          // rows of the stored array (rowwise: the buffer's rows; columnwise: its cols)
+    int64_t row_bytes;     // bytes per stored row
+};
+enum NvGemmKind { NV_FPROP = 0, NV_DGRAD = 1, NV_WGRAD = 2 };
+gq_status launch_gemm_nv(NvGemmKind kind, const NvOperand& a, const NvOperand& b, const int32_t* splits, int G,
+                         int64_t rows_cap, int64_t n, int64_t k, void* out, int out_dtype, int accumulate,
+                         int32_t* status, cudaStream_t stream);
+
 }  // namespace gq

@@ -153,3 +153,61 @@ def test_binding_refuses_host_tensors(lib):
     x = torch.zeros((128, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         gq._ptr(x, "x")
+
+
+def test_descriptor_mirror_matches_the_c_layout(tmp_path):
+    """The ctypes mirror of gq_quantized has the C struct's size and field
+    offsets (gcc compiles a probe against include/gq.h on the host)."""
+    names = [f[0] for f in gq.Quantized._fields_]
+    src = tmp_path / "probe.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"gq.h\"\nint main(void){\n"
+                   + "printf(\"%zu\\n\", sizeof(gq_quantized));\n"
+                   + "".join(f"printf(\"%zu\\n\", offsetof(gq_quantized, {n}));\n" for n in names)
+                   + "return 0;}\n")
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), "-o", str(exe), str(src)], check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert vals[0] == C.sizeof(gq.Quantized)
+    for n, off in zip(names, vals[1:]):
+        assert getattr(gq.Quantized, n).offset == off, n
+
+
+def test_nvfp4_scale_bound_and_host_checks(lib):
+    nv = gq.Recipe(gq.RECIPE_NVFP4_1X16, 1, 1, 0.0)
+    assert gq.gq_scale_bytes_bound(nv, 64, 66560, 7168) == 512 * 112 * (520 + 64)
+    fake = C.c_void_p(0x10000)
+    st = C.c_void_p(0x20000)
+    d = _desc(2, 256, 256, kind=gq.RECIPE_NVFP4_1X16)
+    d.row_data = d.row_scale = d.col_data = d.col_scale = 0x30000
+    d.row_scale_bytes = d.col_scale_bytes = 1 << 20
+    # no amax buffer
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(nv), C.byref(d), st, None) == -1
+    d.amax = 0x40002                                                     # not 4-byte aligned
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(nv), C.byref(d), st, None) == -2
+    d.amax = 0x40000
+    d2 = _desc(2, 240, 256, kind=gq.RECIPE_NVFP4_1X16)                   # colwise needs rows_cap % 32
+    d2.row_data = d2.row_scale = d2.col_data = d2.col_scale = 0x30000
+    d2.row_scale_bytes = d2.col_scale_bytes = 1 << 20
+    d2.amax = 0x40000
+    assert lib.gq_quantize(fake, 240, 256, None, 2, C.byref(nv), C.byref(d2), st, None) == -2
+    d.row_scale_bytes = 16                                               # scale capacity
+    assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(nv), C.byref(d), st, None) == -1
+    # GEMMs: NVFP4 needs n and k multiples of 256, and both operands NVFP4
+    x = _desc(2, 256, 128, kind=gq.RECIPE_NVFP4_1X16)
+    w = _desc(2, 256, 128, kind=gq.RECIPE_NVFP4_1X16)
+    for q in (x, w):
+        q.row_data = q.row_scale = q.col_data = q.col_scale = 0x30000
+        q.row_scale_bytes = q.col_scale_bytes = 1 << 20
+        q.amax = 0x40000
+    y = C.c_void_p(0x50000)
+    assert lib.gq_gemm_fprop(C.byref(x), C.byref(w), None, 2, 128, 128, y, 0, st, None) == -4
+    assert lib.gq_gemm_dgrad(C.byref(x), C.byref(w), None, 2, 128, 128, y, 0, st, None) == -4
+    assert lib.gq_gemm_wgrad(C.byref(x), C.byref(x), None, 2, 128, 128, y, 0, None, 0, st, None) == -4
+    mx = _desc(2, 256, 256)
+    x256 = _desc(2, 256, 256, kind=gq.RECIPE_NVFP4_1X16)
+    x256.row_data = x256.row_scale = 0x30000
+    x256.row_scale_bytes = 1 << 20
+    x256.amax = 0x40000
+    assert lib.gq_gemm_fprop(C.byref(x256), C.byref(mx), None, 2, 128, 256, y, 0, st, None) in (-4, -7)
+    # bias with NVFP4 operands is not provided
+    assert lib.gq_gemm_fprop_bias(C.byref(x), C.byref(w), None, 2, 256, 256, y, 0, y, 0, st, None) == -4
