@@ -42,6 +42,8 @@ if ROOT not in sys.path:
 METRIC = "grouped FP8 GEMM TFLOP/s + quantize GB/s on 1 GB300, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MXFP8_OVER_BF16 = 2.0      # nominal dense ratio: 4.5 vs 2.25 PFLOP/s
+NVFP4_OVER_BF16 = 6.0      # nominal dense ratio: 13.5 vs 2.25 PFLOP/s
+NVFP4_QUANT_BYTES = 5.125  # per element: amax read 2 + cast read 2 + row/col codes 0.5 + 0.5 + scales 2/16
 
 # DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)
 # is measured once on this step and kept in a table under profiles/, each row
@@ -51,6 +53,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_moe_e64_zipf_step.md")
 KERNEL_SOURCES = {
     "gemm": ["gq_gemm.cu", "gq_ptx.cuh", "gq_device.cuh", "gq_internal.h", "gq_host.cu"],
     "quant": ["gq_quant.cu", "gq_ptx.cuh", "gq_device.cuh", "gq_internal.h", "gq_host.cu"],
+    "nvfp4": ["gq_nvfp4.cu", "gq_ptx.cuh", "gq_device.cuh", "gq_internal.h", "gq_host.cu"],
 }
 
 
@@ -71,7 +74,7 @@ def measured_traffic(name: str, kind: str):
             lines = fh.read().splitlines()
     except OSError:
         return None
-    want = source_digest("quant" if kind == "q" else "gemm")
+    want = source_digest("nvfp4" if name.startswith("nv_") else "quant" if kind == "q" else "gemm")
     for line in lines:
         cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
         if len(cells) >= 6 and cells[0] == name:
@@ -96,6 +99,7 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay measurement of the step")
     ap.add_argument("--json-out", default=None)
+    ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 leg of the step")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: the single grouped weight quantisation and the token-count "
                          "sweep (hidden 4096, 32 experts, expert width 1536), as a table")
@@ -411,14 +415,66 @@ class Step:
         cur.wait_stream(self.s_down)
 
 
-def summarize(step, events, peaks, peak_kind):
+class NvStep:
+    """The same fc1/fc2 step on NVFP4 operands (the recipe's second quantiser):
+    the MX step's bf16 inputs and output buffers, NVFP4 quantised buffers of
+    its own; each gq_quantize is three kernels (split scan + amax reset,
+    per-group amax, codes)."""
+
+    def __init__(self, step):
+        gq, torch = step.gq, step.torch
+        self.torch = torch
+        E, H, F, R, L = step.E, step.H, step.F, step.R, step.L
+        nv = gq.Recipe(gq.RECIPE_NVFP4_1X16, 1, 1, 0.0)
+        dev = step.dev
+        q = {"x1": gq.alloc_quantized(R, H, E, nv, dev), "x2": gq.alloc_quantized(R, F, E, nv, dev),
+             "dy1": gq.alloc_quantized(R, F, E, nv, dev), "dy2": gq.alloc_quantized(R, H, E, nv, dev),
+             "w1": gq.alloc_quantized(E * F, H, E, nv, dev), "w2": gq.alloc_quantized(E * H, F, E, nv, dev)}
+        self.q = q
+        i, o, sp, st = step.inputs, step.out, step.splits, step.status
+        live_groups = int(np.count_nonzero(step.wl.splits))
+        bf16 = gq.DTYPE_BF16
+        wb = L * (H + F) * (0.5 + 1 / 16)                  # both columnwise operands of a wgrad
+        self.launches = [
+            ("nv_quant_x1", "q", lambda: gq.gq_quantize(i["x1"], sp, E, nv, q["x1"], st), NVFP4_QUANT_BYTES * L * H),
+            ("nv_quant_w1", "q", lambda: gq.gq_quantize(i["w1"], None, E, nv, q["w1"], st),
+             NVFP4_QUANT_BYTES * E * F * H),
+            ("nv_fprop1", "g", lambda: gq.gq_gemm_fprop(q["x1"], q["w1"], sp, E, F, H, o["y1"], bf16, st),
+             (2.0 * L * F * H, None)),
+            ("nv_quant_x2", "q", lambda: gq.gq_quantize(i["x2"], sp, E, nv, q["x2"], st), NVFP4_QUANT_BYTES * L * F),
+            ("nv_quant_w2", "q", lambda: gq.gq_quantize(i["w2"], None, E, nv, q["w2"], st),
+             NVFP4_QUANT_BYTES * E * H * F),
+            ("nv_fprop2", "g", lambda: gq.gq_gemm_fprop(q["x2"], q["w2"], sp, E, H, F, o["y2"], bf16, st),
+             (2.0 * L * H * F, None)),
+            ("nv_quant_dy2", "q", lambda: gq.gq_quantize(i["dy2"], sp, E, nv, q["dy2"], st),
+             NVFP4_QUANT_BYTES * L * H),
+            ("nv_dgrad2", "g", lambda: gq.gq_gemm_dgrad(q["dy2"], q["w2"], sp, E, H, F, o["dx2"], bf16, st),
+             (2.0 * L * H * F, None)),
+            ("nv_wgrad2", "g", lambda: gq.gq_gemm_wgrad(q["dy2"], q["x2"], sp, E, H, F, o["dw2"], True, st,
+                                                        workspace=None),
+             (2.0 * L * H * F, wb + live_groups * H * F * 8.0)),
+            ("nv_quant_dy1", "q", lambda: gq.gq_quantize(i["dy1"], sp, E, nv, q["dy1"], st),
+             NVFP4_QUANT_BYTES * L * F),
+            ("nv_dgrad1", "g", lambda: gq.gq_gemm_dgrad(q["dy1"], q["w1"], sp, E, F, H, o["dx1"], bf16, st),
+             (2.0 * L * F * H, None)),
+            ("nv_wgrad1", "g", lambda: gq.gq_gemm_wgrad(q["dy1"], q["x1"], sp, E, F, H, o["dw1"], True, st,
+                                                        workspace=None),
+             (2.0 * L * F * H, wb + live_groups * F * H * 8.0)),
+        ]
+        self.gemm_flops = sum(u[0] for _, k, _, u in self.launches if k == "g")
+        self.kernels_per_step = sum(3 if k == "q" else 1 for _, k, _, _ in self.launches)
+
+    run = Step.run
+
+
+def summarize(step, events, peaks, peak_kind, tc_ratio=MXFP8_OVER_BF16):
     """Per-kernel average duration and roofline fraction."""
     by = {}
     for name, a, b in events:
         by.setdefault(name, []).append(a.elapsed_time(b))
     hbm = float(peaks["hbm_gbs"])
-    tc_burst = float(peaks["bf16_tflops"]) * MXFP8_OVER_BF16
-    tc_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * MXFP8_OVER_BF16
+    tc_burst = float(peaks["bf16_tflops"]) * tc_ratio
+    tc_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * tc_ratio
     rows = {}
     for name, kind, _, units in step.launches:
         ms = float(np.mean(by[name]))
@@ -688,6 +744,46 @@ def main():
                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h)}
 
+    # the NVFP4 recipe on the same step (timed on its own, after the MX step)
+    nvfp4 = None
+    if not args.no_nvfp4:
+        nst = NvStep(step)
+        for _ in range(3):
+            nst.run()
+        torch.cuda.synchronize()
+        nsteps = min(args.steps, 10)
+        nev = []
+        dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(nsteps):
+            nst.run(nev)
+        b.record()
+        torch.cuda.synchronize()
+        dist.barrier()
+        if int(step.status.item()) != 0:
+            raise SystemExit("device status set in the NVFP4 region")
+        n_ms = dist.max(a.elapsed_time(b)) / nsteps
+        nrows = summarize(nst, nev, peaks, peak_kind, NVFP4_OVER_BF16)
+        ndom = max(nrows, key=lambda k: nrows[k]["ms"])
+        nd = nrows[ndom]
+        nq_ms = sum(nrows[n]["ms"] for n, k, _, _ in nst.launches if k == "q")
+        ng_ms = sum(nrows[n]["ms"] for n, k, _, _ in nst.launches if k == "g")
+        nq_bytes = sum(u for n, k, _, u in nst.launches if k == "q")
+        nvfp4 = {"value": round(job_value(nst.gemm_flops, dist.world, n_ms) / 1e12, 2), "unit": "TFLOP/s",
+                 "ms_per_step": round(n_ms, 4), "steps": nsteps,
+                 "dtype": "e2m1 NVFP4 (16-element e4m3 scales, per-group fp32 scale; f32 accumulate)",
+                 "workload": "moe_e64_zipf fc1+fc2 on NVFP4 operands (same inputs as the MX step)",
+                 "quantize_gbs": round(nq_bytes / (nq_ms * 1e-3) / 1e9, 1),
+                 "quantize_frac_hbm": round(nq_bytes / (nq_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4),
+                 "gemm_tflops": round(nst.gemm_flops / (ng_ms * 1e-3) / 1e12, 1),
+                 "roofline": {"kernel": ndom, "bound": nd["bound"], "achieved": nd["achieved"], "peak": nd["peak"],
+                              "unit": nd["unit"], "frac": nd["frac"], "traffic": nd["traffic"],
+                              "peak_source": f"{peak_kind} ({'hbm_gbs' if nd['bound'] == 'hbm' else 'bf16_tflops x 6 (NVFP4/bf16 nominal ratio)'})"},
+                 "breakdown": nrows, "gpu_launches": nst.kernels_per_step * nsteps}
+        del nst
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -706,7 +802,7 @@ def main():
         "quantize_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(qbytes / (qms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4),
         "gemm_tflops": round(step.gemm_flops / (gms * 1e-3) / 1e12, 1),
-        "roofline": roof, "breakdown": rows, "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
+        "roofline": roof, "breakdown": rows, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "nvfp4": nvfp4,
         "gpu_launches": len(step.launches) * args.steps, "clocks": clk,
     }
     if dist.rank == 0:

@@ -78,30 +78,79 @@ __device__ __forceinline__ float nv_alpha(float amax_a, float amax_b)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// One block of 16 values: its E4M3 scale byte and its 16 codes (element i in
-// nibble i of the 64-bit word, i.e. byte i / 2, low nibble for even i).
-__device__ __forceinline__ uint32_t nv_encode16(const float (&x)[16], float S, uint2& codes)
+// amax / 6 rounded to nearest even for a bf16 amax, without a division:
+// q1 = amax * RN(1/6), then one correction step q1 + (amax - 6 q1) * RN(1/6)
+// with fused multiply-adds (Markstein's correction of a reciprocal product).
+// Checked against the correctly rounded quotient for every finite bf16
+// magnitude, subnormals included.
+__device__ __forceinline__ float div6_bf16(float amax)
 {
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        amax = fmaxf(amax, fabsf(x[i]));
-    const float s = __fmul_rn(__fdiv_rn(amax, 6.f), S);
+    const float y = 0x1.555556p-3f;               // RN(1/6)
+    const float q1 = __fmul_rn(amax, y);
+    const float r = __fmaf_rn(-q1, 6.f, amax);
+    return __fmaf_rn(r, y, q1);
+}
+
+// The quantiser's per-tile table m[sf] = S_g / sf (0 for sf = 0, clamped to
+// FLT_MAX) over the 127 non-negative finite E4M3 bytes, so that a block
+// needs no division.
+__device__ __forceinline__ float nv_encode_mult(float S, uint32_t sf)
+{
+    if (sf == 0)
+        return 0.f;
+    const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sf, __NV_E4M3)));
+    return fminf(__fdiv_rn(S, d), FLT_MAX);
+}
+
+// Eight values as E2M1 codes in one word, element 2i of the pairs in nibble
+// 2i (round to nearest even, saturating): the converting instruction puts its
+// first source in the high nibble of its byte.
+__device__ __forceinline__ uint32_t e2m1x8(float2 a, float2 b, float2 c, float2 d)
+{
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+    return w;
+}
+
+// Halfwise maximum of two bf16 pairs (non-negative values: exact).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    const __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// One block of 16 values whose amax (an fp32 widened from bf16) is known:
+// its E4M3 scale byte and its 16 codes (element i in nibble i of the 64-bit
+// word, i.e. byte i / 2, low nibble for even i).
+__device__ __forceinline__ uint32_t nv_encode16_t(const float (&x)[16], float amax, float S, const float* mtab,
+                                                  uint2& codes)
+{
+    const float s = __fmul_rn(div6_bf16(amax), S);
     const uint32_t sf = __nv_cvt_float_to_fp8(s, __NV_SATFINITE, __NV_E4M3);
-    float m = 0.f;
-    if (sf != 0) {
-        const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sf, __NV_E4M3)));
-        m = fminf(__fdiv_rn(S, d), FLT_MAX);
-    }
-    uint32_t w[2] = {0u, 0u};
+    const float m = mtab[sf];
+    float2 p[8];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        const uint32_t c = __nv_cvt_float2_to_fp4x2(make_float2(__fmul_rn(x[i], m), __fmul_rn(x[i + 1], m)),
-                                                    __NV_E2M1, cudaRoundNearest);
-        w[i / 8] |= (c & 0xffu) << (4 * (i % 8));
-    }
-    codes = make_uint2(w[0], w[1]);
+    for (int i = 0; i < 8; ++i)
+        p[i] = __fmul2_rn(make_float2(x[2 * i], x[2 * i + 1]), make_float2(m, m));
+    codes = make_uint2(e2m1x8(p[0], p[1], p[2], p[3]), e2m1x8(p[4], p[5], p[6], p[7]));
     return sf;
+}
+
+// Largest bf16 magnitude among the 2 x 4 halves of two 16-byte words, as fp32.
+__device__ __forceinline__ float amax16_bf16(const uint4& a, const uint4& b)
+{
+    constexpr uint32_t M = 0x7fff7fffu;
+    uint32_t m = bmax2(bmax2(a.x & M, a.y & M), bmax2(a.z & M, a.w & M));
+    m = bmax2(m, bmax2(bmax2(b.x & M, b.y & M), bmax2(b.z & M, b.w & M)));
+    return __uint_as_float(max(m & 0xffffu, m >> 16) << 16);
 }
 
 // Largest g in [0, G) with s_off[g] <= r: the group that owns live row r
@@ -204,111 +253,231 @@ __global__ void __launch_bounds__(256) k_nv_amax(const uint16_t* __restrict__ x,
     }
 }
 
-constexpr int kNqThreads = 256;
-constexpr int kNqPitch = 128 * 2 + 16;             // bytes per bf16 tile row in shared memory
-constexpr int kNqTile = 128 * kNqPitch;
-constexpr int kNqSmem = kNqTile + 2 * 128 * 64 + 4 * 512 + kScanBytes + 16;
+// Shared-memory plan of k_nv_quant: a ring of kNqStages bf16 input tiles
+// (128 rows x 128 columns, two 128-byte-swizzled TMA boxes of [128 rows][64
+// columns]) with the tile's table m[sf]; two output staging buffers (the
+// columnwise codes [128 columns][64 bytes] and the tile's four atoms); the
+// ring's barriers; the split scan.
+constexpr int kNqStages = 5;
+constexpr int kNqTile = 128 * 128 * 2;
+constexpr int kNqConsumers = 512;                     // 16 consumer warps
+constexpr int kNqThreads = kNqConsumers + 32;         // + 1 producer warp
+constexpr int kNqOut = 128 * 64 + 4 * 512;
+constexpr int kNqSmem = 1024 + kNqStages * kNqTile + kNqStages * 512 + 2 * kNqOut + 2 * 8 * kNqStages + 16 + kScanBytes;
 
-// One step = one 128-row x 128-column tile of one group (the group's own
-// 128-row tiles, so one S_g per tile): the bf16 tile is staged in shared
-// memory; rowwise blocks (a row's 16 columns) and columnwise blocks (a
-// column's 16 rows) are encoded from there; codes and the tile's two rowwise
-// and two columnwise atoms are staged in shared memory and leave as 16-byte
-// chunks.  Only live rows are read or written.
-template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kNqThreads) k_nv_quant(const uint16_t* __restrict__ x, int64_t rows_cap,
-                                                         int64_t cols, const int32_t* splits, int G,
-                                                         const float* __restrict__ amax, uint8_t* row_data,
-                                                         uint8_t* row_scale, uint8_t* col_data, uint8_t* col_scale,
-                                                         int32_t* status)
+// Tile order of the quantiser (tuning knob): tiles are walked in bands of
+// GQ_NQ_BAND row tiles, row tile fastest inside a band, so that the CTAs
+// working at the same time cover a few row tiles x many column tiles: the
+// rowwise codes (64 bytes a row per tile) and the transposed columnwise codes
+// (64 bytes a column per tile) both leave in runs of adjacent segments.
+#ifndef GQ_NQ_BAND
+#define GQ_NQ_BAND 8
+#endif
+constexpr int kNqBand = GQ_NQ_BAND;
+
+// One 128 x 128 tile of one group (the group's own 128-row tiles, so one S_g
+// per tile).
+struct NqTile {
+    int g;
+    int rows;          // live rows (a multiple of 32)
+    int64_t mt, ct;    // row tile in the group, column tile
+    int64_t row0;      // first buffer row
+};
+
+__device__ __forceinline__ NqTile nq_tile(const Scan& sc, int G, int64_t nct, int64_t t)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t* tile = smem;
-    uint8_t* rcodes = tile + kNqTile;              // [128 rows][64 bytes]
-    uint8_t* ccodes = rcodes + 128 * 64;           // [128 columns][64 bytes]
-    uint8_t* atoms = ccodes + 128 * 64;            // rowwise atoms 0, 1; columnwise atoms 2, 3
+    NqTile q;
+    const int64_t band = t / (kNqBand * nct);
+    const int64_t rt0 = band * kNqBand;
+    const int64_t nb = min((int64_t)kNqBand, (int64_t)sc.tp[G] - rt0);     // row tiles of this band
+    const int64_t u = t - band * kNqBand * nct;
+    const int64_t rt = rt0 + u % nb;
+    q.ct = u / nb;
+    q.g = group_of_tile(sc.tp, G, rt);
+    q.mt = rt - sc.tp[q.g];
+    q.rows = (int)min((int64_t)128, (int64_t)(sc.off[q.g + 1] - sc.off[q.g]) - 128 * q.mt);
+    q.row0 = sc.off[q.g] + 128 * q.mt;
+    return q;
+}
+
+// Byte address of bf16 element (r, 4 p') of a 128-byte-swizzled tile, for the
+// 4-byte column pair p (columns 2 p, 2 p + 1) of row r.
+__device__ __forceinline__ uint32_t nq_pair_addr(uint32_t tile, int r, int p)
+{
+    const int h = p >> 5, j = (p & 31) >> 2;
+    return tile + h * 16384 + r * 128 + ((j ^ (r & 7)) << 4) + 4 * (p & 3);
+}
+
+// Warp roles: warp 16 is the producer -- per tile it waits for a free stage,
+// writes the tile's m[sf] table (its 32 lanes), and lane 0 issues the TMA
+// loads of the tile's live rows (whole 128-row boxes, or 32-row boxes for a
+// group's last tile, so rows past the live total are never read).  Warps
+// 0..15 are the consumers: rowwise items (row, 16-column block) send their 8
+// code bytes straight to global memory; columnwise items (column pair,
+// 16-row block) stage theirs; one named barrier per tile, after which the
+// stage goes back to the producer and the staged codes and atoms leave as
+// 16-byte chunks (double-buffered staging, so one barrier suffices).
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kNqThreads, 1)
+k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ CUtensorMap map32, int64_t rows_cap,
+           int64_t cols, const int32_t* splits, int G, const float* __restrict__ amax, uint8_t* row_data,
+           uint8_t* row_scale, uint8_t* col_data, uint8_t* col_scale, int32_t* status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* mtabs = reinterpret_cast<float*>(tiles + kNqStages * kNqTile);     // [stage][128]
+    uint8_t* outs = reinterpret_cast<uint8_t*>(mtabs + kNqStages * 128);     // [2][ccodes | atoms]
+    uint64_t* full = reinterpret_cast<uint64_t*>(outs + 2 * kNqOut);
+    uint64_t* empty = full + kNqStages;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + kNqStages);
     if (load_status(status) != 0)
         return;
-    const Scan sc = carve_scan(atoms + 4 * 512);
+    const Scan sc = carve_scan(reinterpret_cast<uint8_t*>(empty + kNqStages) + 16);
     if (block_scan_splits(splits, G, rows_cap, 32, sc.off, sc.tp, sc.w64, sc.w32))
         return;                                  // reported by k_nv_prepare
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kNqStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        *abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
     const int64_t nct = cols / 128;
     const int64_t ntiles = (int64_t)sc.tp[G] * nct;
-    const int tid = threadIdx.x;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int64_t rt = t / nct, ct = t - rt * nct;
-        const int g = group_of_tile(sc.tp, G, rt);
-        const int64_t mt = rt - sc.tp[g];
-        const int64_t T = sc.tp[g + 1] - sc.tp[g];
-        const int rows = (int)min((int64_t)128, (int64_t)(sc.off[g + 1] - sc.off[g]) - 128 * mt);
-        const int64_t row0 = sc.off[g] + 128 * mt;
-        const float S = nv_global_scale(__ldg(amax + g));
-        for (int i = tid; i < rows * 16; i += kNqThreads) {
-            const int r = i >> 4, ch = i & 15;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (row0 + r) * cols + ct * 128) + ch);
-            *reinterpret_cast<uint4*>(tile + r * kNqPitch + ch * 16) = v;
+
+    if (warp == kNqConsumers / 32) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            ptx::prefetch_tmap(&map128);
+            ptx::prefetch_tmap(&map32);
         }
-        __syncthreads();
+        int s = 0;
+        uint32_t ph = 0;
+        int64_t issued = 0;
+        for (int64_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+            if (!ptx::mbar_wait_warp(&empty[s], ph ^ 1u, abort, status))
+                break;
+            const NqTile q = nq_tile(sc, G, nct, t);
+            const float S = nv_global_scale(__ldg(amax + q.g));
+            // entry 127 (an E4M3 NaN byte, never a scale) carries S_g itself
+            for (int e = lane; e < 128; e += 32)
+                mtabs[s * 128 + e] = e == 127 ? S : nv_encode_mult(S, (uint32_t)e);
+            __syncwarp();
+            if (lane == 0) {
+                uint8_t* dst = tiles + s * kNqTile;
+                ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(q.rows * 256));
+                const int32_t x0 = (int32_t)(q.ct * 128);
+                if (q.rows == 128) {
+                    ptx::tma_load_2d(dst, &map128, &full[s], x0, (int32_t)q.row0);
+                    ptx::tma_load_2d(dst + 16384, &map128, &full[s], x0 + 64, (int32_t)q.row0);
+                } else {
+                    for (int r = 0; r < q.rows; r += 32) {
+                        ptx::tma_load_2d(dst + r * 128, &map32, &full[s], x0, (int32_t)(q.row0 + r));
+                        ptx::tma_load_2d(dst + 16384 + r * 128, &map32, &full[s], x0 + 64, (int32_t)(q.row0 + r));
+                    }
+                }
+            }
+            ++issued;
+            if (++s == kNqStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        if (lane == 0) {
+            // loads in flight after an abort land before the CTA leaves
+            volatile int no_abort = 0;
+            for (int64_t k = issued - kNqStages < 0 ? 0 : issued - kNqStages; k < issued; ++k)
+                if (!ptx::mbar_wait(&full[k % kNqStages], (uint32_t)((k / kNqStages) & 1), &no_abort, status))
+                    break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers --
+    int s = 0, ob = 0;
+    uint32_t ph = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const bool ok = ptx::mbar_wait_warp(&full[s], ph, abort, status);
+        if (ptx::named_barrier_or(1, kNqConsumers, !ok))
+            break;
+        const NqTile q = nq_tile(sc, G, nct, t);
+        const int rows = q.rows;
+        const uint32_t tile = ptx::smem_addr(tiles + s * kNqTile);
+        const float* mtab = mtabs + s * 128;
+        const float S = mtab[127];
+        uint8_t* ccodes = outs + ob * kNqOut;
+        uint8_t* atoms = ccodes + 128 * 64;
         if (ROW) {
-            for (int i = tid; i < 128 * 8; i += kNqThreads) {
-                const int r = i >> 3, j = i & 7;       // row, 16-column block
+            for (int i = tid; i < 128 * 8; i += kNqConsumers) {
+                const int r = i >> 3, jb = i & 7;       // row, 16-column block
                 uint32_t sf = 0;
                 if (r < rows) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(tile + r * kNqPitch + j * 32);
-                    const uint4 b = *reinterpret_cast<const uint4*>(tile + r * kNqPitch + j * 32 + 16);
+                    const int h = jb >> 2, j = 2 * (jb & 3);
+                    const uint32_t rowa = tile + h * 16384 + r * 128;
+                    const uint4 a = ptx::lds128(rowa + ((j ^ (r & 7)) << 4));
+                    const uint4 b = ptx::lds128(rowa + (((j + 1) ^ (r & 7)) << 4));
                     const float v[16] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
                                          bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w),
                                          bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
                                          bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
                     uint2 cw;
-                    sf = nv_encode16(v, S, cw);
-                    *reinterpret_cast<uint2*>(rcodes + r * 64 + j * 8) = cw;
+                    sf = nv_encode16_t(v, amax16_bf16(a, b), S, mtab, cw);
+                    *reinterpret_cast<uint2*>(row_data + (q.row0 + r) * (cols / 2) + q.ct * 64 + jb * 8) = cw;
                 }
-                atoms[(j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3)] = (uint8_t)sf;
+                atoms[(jb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (jb & 3)] = (uint8_t)sf;
             }
         }
         if (COL) {
-            for (int i = tid; i < 128 * 8; i += kNqThreads) {
-                const int c = i & 127, b = i >> 7;     // column, 16-row block
-                uint32_t sf = 0;
-                if (16 * b < rows) {
-                    float v[16];
+            const int p = tid & 63, b = tid >> 6;      // column pair, 16-row block (512 items)
+            uint32_t sf0 = 0, sf1 = 0;
+            if (16 * b < rows) {
+                float v0[16], v1[16];
+                uint32_t m = 0;
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        v[k] = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                                   tile + (16 * b + k) * kNqPitch + 2 * c)
-                                               << 16);
-                    uint2 cw;
-                    sf = nv_encode16(v, S, cw);
-                    *reinterpret_cast<uint2*>(ccodes + c * 64 + b * 8) = cw;
+                for (int k = 0; k < 16; ++k) {
+                    uint32_t wd;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wd) : "r"(nq_pair_addr(tile, 16 * b + k, p)));
+                    v0[k] = bf16_lo(wd);
+                    v1[k] = bf16_hi(wd);
+                    m = bmax2(m, wd & 0x7fff7fffu);
                 }
-                atoms[(2 + (b >> 2)) * 512 + (c & 31) * 16 + (c >> 5) * 4 + (b & 3)] = (uint8_t)sf;
+                uint2 c0, c1;
+                sf0 = nv_encode16_t(v0, __uint_as_float((m & 0xffffu) << 16), S, mtab, c0);
+                sf1 = nv_encode16_t(v1, __uint_as_float(m & 0xffff0000u), S, mtab, c1);
+                *reinterpret_cast<uint2*>(ccodes + (2 * p) * 64 + b * 8) = c0;
+                *reinterpret_cast<uint2*>(ccodes + (2 * p + 1) * 64 + b * 8) = c1;
             }
+            const int c = 2 * p;
+            atoms[(2 + (b >> 2)) * 512 + (c & 31) * 16 + (c >> 5) * 4 + (b & 3)] = (uint8_t)sf0;
+            atoms[(2 + (b >> 2)) * 512 + ((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + (b & 3)] = (uint8_t)sf1;
         }
-        __syncthreads();
-        const int64_t sb = 512 * (cols / 64) * (int64_t)sc.tp[g];
-        if (ROW) {
-            for (int i = tid; i < rows * 4; i += kNqThreads) {
-                const int r = i >> 2, ch = i & 3;
-                *reinterpret_cast<uint4*>(row_data + (row0 + r) * (cols / 2) + ct * 64 + ch * 16) =
-                    *reinterpret_cast<const uint4*>(rcodes + r * 64 + ch * 16);
-            }
-            if (tid < 64)
-                *reinterpret_cast<uint4*>(row_scale + sb + (mt * (cols / 64) + 2 * ct) * 512 + tid * 16) =
-                    *reinterpret_cast<const uint4*>(atoms + tid * 16);
-        }
+        ptx::named_barrier_or(1, kNqConsumers, 0);
+        if (tid == 0)
+            ptx::mbar_arrive(&empty[s]);
+        const int64_t sb = 512 * (cols / 64) * (int64_t)sc.tp[q.g];
+        if (ROW && tid < 64)
+            *reinterpret_cast<uint4*>(row_scale + sb + (q.mt * (cols / 64) + 2 * q.ct) * 512 + tid * 16) =
+                *reinterpret_cast<const uint4*>(atoms + tid * 16);
         if (COL) {
+            const int64_t T = sc.tp[q.g + 1] - sc.tp[q.g];
             const int nch = rows / 32;                 // 16-byte chunks of a column (rows / 2 bytes)
-            for (int i = tid; i < 128 * nch; i += kNqThreads) {
+            for (int i = tid; i < 128 * nch; i += kNqConsumers) {
                 const int c = i / nch, ch = i - c * nch;
-                *reinterpret_cast<uint4*>(col_data + (ct * 128 + c) * (rows_cap / 2) + row0 / 2 + ch * 16) =
+                *reinterpret_cast<uint4*>(col_data + (q.ct * 128 + c) * (rows_cap / 2) + q.row0 / 2 + ch * 16) =
                     *reinterpret_cast<const uint4*>(ccodes + c * 64 + ch * 16);
             }
             if (tid >= 64 && tid < 128)
-                *reinterpret_cast<uint4*>(col_scale + sb + (ct * 2 * T + 2 * mt) * 512 + (tid - 64) * 16) =
+                *reinterpret_cast<uint4*>(col_scale + sb + (q.ct * 2 * T + 2 * q.mt) * 512 + (tid - 64) * 16) =
                     *reinterpret_cast<const uint4*>(atoms + 1024 + (tid - 64) * 16);
         }
-        __syncthreads();
+        ob ^= 1;
+        if (++s == kNqStages) {
+            s = 0;
+            ph ^= 1u;
+        }
     }
 }
 
@@ -773,24 +942,27 @@ cudaError_t launch_quant_nv(const void* x, int64_t rows_cap, int64_t cols, const
         xb, rows_cap, cols, splits, G, amax, status);
     if (cudaGetLastError() != cudaSuccess)
         return cudaErrorLaunchFailure;
+    CUtensorMap m128, m32;
+    if (!make_tensor_map_2d(&m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows_cap, cols, 64, 128) ||
+        !make_tensor_map_2d(&m32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows_cap, cols, 64, 32))
+        return cudaErrorInvalidValue;
     const void* fn = row_data && col_data ? reinterpret_cast<const void*>(k_nv_quant<true, true>)
                      : row_data           ? reinterpret_cast<const void*>(k_nv_quant<true, false>)
                                           : reinterpret_cast<const void*>(k_nv_quant<false, true>);
-    int per_sm = 1;
-    const cudaError_t e = prepare_kernel(fn, kNqSmem, kNqThreads, &per_sm);
+    const cudaError_t e = prepare_kernel(fn, kNqSmem, kNqThreads, nullptr);
     if (e != cudaSuccess)
         return e;
     const int64_t tiles_bound = ((rows_cap + 127) / 128 + G) * (cols / 128);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * std::max(per_sm, 1), tiles_bound));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms, tiles_bound));
     if (row_data && col_data)
         k_nv_quant<true, true><<<(unsigned)grid, kNqThreads, kNqSmem, stream>>>(
-            xb, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
+            m128, m32, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
     else if (row_data)
         k_nv_quant<true, false><<<(unsigned)grid, kNqThreads, kNqSmem, stream>>>(
-            xb, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
+            m128, m32, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
     else
         k_nv_quant<false, true><<<(unsigned)grid, kNqThreads, kNqSmem, stream>>>(
-            xb, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
+            m128, m32, rows_cap, cols, splits, G, amax, row_data, row_scale, col_data, col_scale, status);
     return cudaGetLastError();
 }
 

@@ -27,6 +27,11 @@ the same live total; --store writes the wgrad result (accumulate = 0)
 instead of adding it to the main grad; --static runs the wgrad in its static
 tile order (no claim workspace).
   wgrad_ch    kgrouped_zero_channel per-channel wgrad (4 x 2048 x 2048)
+  nv_quant    NVFP4 row+col quantisation of the moe_e64_zipf fc1 input
+              (three kernels: split scan + amax reset, amax, codes)
+  nv_fprop    moe_e64_zipf fc1 fprop on NVFP4 operands (bf16 output)
+  nv_dgrad    moe_e64_zipf fc1 dgrad on NVFP4 operands (bf16 output)
+  nv_wgrad    moe_e64_zipf fc1 wgrad on NVFP4 operands, accumulating into fp32
 Prints the mean CUDA-event time per launch.
 """
 from __future__ import annotations
@@ -43,7 +48,8 @@ if ROOT not in sys.path:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad64",
-                                     "wgrad_ch", "fprop_bias", "quant_dbias", "fprop_act"])
+                                     "wgrad_ch", "fprop_bias", "quant_dbias", "fprop_act", "nv_quant",
+                                     "nv_fprop", "nv_dgrad", "nv_wgrad"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--uniform", action="store_true")
     ap.add_argument("--store", action="store_true")
@@ -73,7 +79,33 @@ def main():
         gq.gq_quantize(t, splits, E, mx, q, st)
         return q
 
-    if args.case == "quant":
+    nv = gq.Recipe(gq.RECIPE_NVFP4_1X16, 1, 1, 0.0)
+
+    def quant_nv(t, splits):
+        q = gq.alloc_quantized(t.shape[0], t.shape[1], E, nv, dev)
+        gq.gq_quantize(t, splits, E, nv, q, st)
+        return q
+
+    if args.case == "nv_quant":
+        x = W.device_activation(w, H, 0, device=dev)
+        q = gq.alloc_quantized(R, H, E, nv, dev)
+        fn = lambda: gq.gq_quantize(x, sp, E, nv, q, st)  # noqa: E731
+    elif args.case in ("nv_fprop", "nv_dgrad", "nv_wgrad"):
+        wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
+        qw = quant_nv(wt, None)
+        del wt
+        qx = quant_nv(W.device_activation(w, H, 0, device=dev), sp)
+        qd = quant_nv(W.device_activation(w, F, 2, device=dev), sp)
+        if args.case == "nv_fprop":
+            y = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_fprop(qx, qw, sp, E, F, H, y, gq.DTYPE_BF16, st)  # noqa: E731
+        elif args.case == "nv_dgrad":
+            dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+            fn = lambda: gq.gq_gemm_dgrad(qd, qw, sp, E, F, H, dx, gq.DTYPE_BF16, st)  # noqa: E731
+        else:
+            dw = W.device_normal_bf16((E, F, H), w.seed, 1e-3, 20, dev).float()
+            fn = lambda: gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, True, st, workspace=None)  # noqa: E731
+    elif args.case == "quant":
         x = W.device_activation(w, H, 0, device=dev)
         q = gq.alloc_quantized(R, H, E, mx, dev)
         fn = lambda: gq.gq_quantize(x, sp, E, mx, q, st)  # noqa: E731

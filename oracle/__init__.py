@@ -92,7 +92,10 @@ def _load():
                                               C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
             lib.or_gemm_nvfp4.argtypes = ([C.c_int] + [C.c_void_p] * 7 +
                                           [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int, C.c_void_p])
-            for name in ("or_quantize_nvfp4", "or_gemm_nvfp4"):
+            lib.or_gemm_nvfp4_sample.argtypes = ([C.c_int] + [C.c_void_p] * 7 +
+                                                 [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
+                                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p])
+            for name in ("or_quantize_nvfp4", "or_gemm_nvfp4", "or_gemm_nvfp4_sample"):
                 getattr(lib, name).restype = C.c_int
             for name in ("or_split_scan", "or_quantize_mx", "or_quantize_channel", "or_srelu_quantize_mx",
                          "or_gemm_fprop", "or_gemm_dgrad", "or_gemm_wgrad_mx",
@@ -331,6 +334,30 @@ def gemm_nvfp4(kind: str, a: NVQuantized, b: NVQuantized, splits, num_groups, N,
                            N, K, int(accumulate), _p(y))
     _check(st, "gemm_nvfp4")
     return y
+
+
+def gemm_nvfp4_sample(kind: str, a: NVQuantized, b: NVQuantized, splits, num_groups, N, K, i_idx, j_idx,
+                      g_idx=None) -> np.ndarray:
+    """Selected outputs of gemm_nvfp4, one fp64 dot product each: 'fprop'
+    (row, n), 'dgrad' (row, k), 'wgrad' (g, n, k) without the accumulate term."""
+    lib = _load()
+    i_idx = np.ascontiguousarray(i_idx, np.int64)
+    j_idx = np.ascontiguousarray(j_idx, np.int64)
+    g = np.ascontiguousarray(np.zeros_like(i_idx) if g_idx is None else g_idx, np.int32)
+    out = np.empty(i_idx.size, np.float64)
+    if kind == "fprop":
+        k, ad, as_, bd, bs = 0, a.row_data, a.row_scale, b.row_data, b.row_scale
+    elif kind == "dgrad":
+        k, ad, as_, bd, bs = 1, a.row_data, a.row_scale, b.col_data, b.col_scale
+    elif kind == "wgrad":
+        k, ad, as_, bd, bs = 2, a.col_data, a.col_scale, b.col_data, b.col_scale
+    else:
+        raise ValueError(kind)
+    st = lib.or_gemm_nvfp4_sample(k, _p(ad), _p(as_), _p(np.ascontiguousarray(a.amax, np.float32)), _p(bd),
+                                  _p(bs), _p(np.ascontiguousarray(b.amax, np.float32)), _p(_splits(splits)),
+                                  num_groups, a.rows_cap, N, K, i_idx.size, _p(g), _p(i_idx), _p(j_idx), _p(out))
+    _check(st, "gemm_nvfp4_sample")
+    return out
 
 
 # --------------------------------------------------------------------------- #

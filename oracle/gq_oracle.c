@@ -1071,3 +1071,54 @@ int or_gemm_nvfp4(int kind, const uint8_t* a_data, const uint8_t* a_scale, const
     free(sb.buf);
     return OR_OK;
 }
+
+/* Sampled outputs of the NVFP4 GEMMs, one fp64 dot product each (kind and
+ * operands as or_gemm_nvfp4; fprop (i = row, j = n), dgrad (i = row, j = k),
+ * wgrad (g, i = n, j = k) without any accumulate term). */
+int or_gemm_nvfp4_sample(int kind, const uint8_t* a_data, const uint8_t* a_scale, const float* a_amax,
+                         const uint8_t* b_data, const uint8_t* b_scale, const float* b_amax, const int32_t* splits,
+                         int G, int64_t rows_cap, int64_t N, int64_t K, int64_t n_samples, const int32_t* g_idx,
+                         const int64_t* i_idx, const int64_t* j_idx, double* out)
+{
+    scan_t sa, sb;
+    int64_t wrows = (int64_t)G * N;
+    int st;
+    if (kind < 0 || kind > 2)
+        return OR_ERR_INVALID_ARG;
+    st = make_layout(&sa, splits, G, rows_cap, kind == 0 ? K : N, OR_RECIPE_MX);
+    if (st != OR_OK)
+        return st;
+    if (kind == 2)
+        st = make_layout(&sb, splits, G, rows_cap, K, OR_RECIPE_MX);
+    else
+        st = make_layout(&sb, NULL, G, wrows, K, OR_RECIPE_MX);
+    if (st != OR_OK) {
+        free(sa.buf);
+        return st;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t s = 0; s < n_samples; ++s) {
+        double acc = 0.0;
+        int64_t i = i_idx[s], j = j_idx[s];
+        if (kind == 0) {
+            int g = group_of_row(&sa.l, i);
+            for (int64_t k = 0; k < K; ++k)
+                acc += nv_elem(&sa.l, rows_cap, a_data, a_scale, a_amax, 0, g, i, k) *
+                       nv_elem(&sb.l, wrows, b_data, b_scale, b_amax, 0, g, (int64_t)g * N + j, k);
+        } else if (kind == 1) {
+            int g = group_of_row(&sa.l, i);
+            for (int64_t n = 0; n < N; ++n)
+                acc += nv_elem(&sa.l, rows_cap, a_data, a_scale, a_amax, 0, g, i, n) *
+                       nv_elem(&sb.l, wrows, b_data, b_scale, b_amax, 1, g, (int64_t)g * N + n, j);
+        } else {
+            int g = g_idx[s];
+            for (int64_t r = sa.l.off[g]; r < sa.l.off[g + 1]; ++r)
+                acc += nv_elem(&sa.l, rows_cap, a_data, a_scale, a_amax, 1, g, r, i) *
+                       nv_elem(&sb.l, rows_cap, b_data, b_scale, b_amax, 1, g, r, j);
+        }
+        out[s] = acc;
+    }
+    free(sa.buf);
+    free(sb.buf);
+    return OR_OK;
+}

@@ -238,3 +238,82 @@ def test_bad_splits_make_every_call_a_noop():
     check_status(st, -3)                                  # GQ_ERR_SPLITS
     assert torch.all(q.row_data == FILL) and torch.all(q.col_data == FILL)
     assert torch.all(q.amax.view(torch.uint8) == FILL)
+
+
+# --------------------------------------------------------------------------- #
+# full size: the large MoE layer in the benchmark's launch configuration      #
+# --------------------------------------------------------------------------- #
+
+def _bits_of(t):
+    return host(t.view(torch.int16)).view(np.uint16)
+
+
+@pytest.mark.parametrize("fc", [1, 2])
+def test_moe_e64_zipf_layer_nvfp4(fc):
+    """E = 64, hidden 7168, ffn 2048, 65536 Zipf-routed tokens + 1024 garbage
+    rows: every quantised buffer byte for byte against the oracle, and fprop,
+    dgrad and wgrad (accumulate into an fp32 main grad) on 4096 sampled
+    outputs each, per-group sampled relative error within 1e-5."""
+    w = W.workload("moe_e64_zipf")
+    E, R, L = w.num_groups, w.rows_cap, w.live_rows
+    K, N = (w.hidden, w.ffn) if fc == 1 else (w.ffn, w.hidden)
+    s = 0 if fc == 1 else 1
+    x = W.device_activation(w, K, 40 + s, device=DEV)
+    dy = W.device_activation(w, N, 42 + s, device=DEV)
+    wt = W.device_normal_bf16((E * N, K), w.seed, 0.02, 44 + s, DEV)
+    main = W.device_normal_bf16((E, N, K), w.seed, 1e-3, 46 + s, DEV).float()
+    main0 = main.clone()
+    sp = torch.as_tensor(w.splits).to(DEV)
+    st = status_dev()
+    rec = nv_recipe()
+    q = {k: gq.alloc_quantized(t.shape[0], t.shape[1], E, rec, DEV, fill=FILL)
+         for k, t in (("x", x), ("dy", dy), ("w", wt))}
+    gq.gq_quantize(x, sp, E, rec, q["x"], st)
+    gq.gq_quantize(dy, sp, E, rec, q["dy"], st)
+    gq.gq_quantize(wt, None, E, rec, q["w"], st)
+    y = torch.empty((R, N), dtype=torch.float32, device=DEV)
+    dx = torch.empty((R, K), dtype=torch.bfloat16, device=DEV)
+    gq.gq_gemm_fprop(q["x"], q["w"], sp, E, N, K, y, gq.DTYPE_F32, st)
+    gq.gq_gemm_dgrad(q["dy"], q["w"], sp, E, N, K, dx, gq.DTYPE_BF16, st)
+    gq.gq_gemm_wgrad(q["dy"], q["x"], sp, E, N, K, main, True, st)
+    torch.cuda.synchronize()
+    check_status(st)
+
+    ox = O.quantize_nvfp4(_bits_of(x), w.splits, E)
+    ody = O.quantize_nvfp4(_bits_of(dy), w.splits, E)
+    ow = O.quantize_nvfp4(_bits_of(wt), None, E)
+    assert_nv_equal(q["x"], ox, L, O.scale_bytes_nvfp4(w.splits, E, R, K))
+    assert_nv_equal(q["dy"], ody, L, O.scale_bytes_nvfp4(w.splits, E, R, N))
+    assert_nv_equal(q["w"], ow, E * N, O.scale_bytes_nvfp4(None, E, E * N, K))
+
+    rng = np.random.default_rng(98)
+    n_s = 4096
+    off = np.concatenate([[0], np.cumsum(w.splits)])
+    rows = rng.integers(0, L, n_s)
+    grp = np.searchsorted(off, rows, side="right") - 1
+    cn, ck = rng.integers(0, N, n_s), rng.integers(0, K, n_s)
+
+    def gather(t, *idx):
+        return host(t[tuple(torch.as_tensor(i).to(DEV) for i in idx)].float()).astype(np.float64)
+
+    def per_group(got, want, groups):
+        errs = []
+        for g in np.unique(groups):
+            m = groups == g
+            nw = np.linalg.norm(want[m])
+            errs.append(np.linalg.norm(got[m] - want[m]) / nw if nw > 0 else float(np.any(got[m] != 0)))
+        return np.array(errs)
+
+    want = O.gemm_nvfp4_sample("fprop", ox, ow, w.splits, E, N, K, rows, cn)
+    assert np.all(per_group(gather(y, rows, cn), want, grp) <= REL_TOL), "fprop"
+    want = O.gemm_nvfp4_sample("dgrad", ody, ow, w.splits, E, N, K, rows, ck)
+    got = gather(dx, rows, ck)
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8 + 1e-6), "dgrad bf16"
+    g = rng.choice(np.flatnonzero(w.splits > 0), n_s)
+    want = O.gemm_nvfp4_sample("wgrad", ody, ox, w.splits, E, N, K, cn, ck, g)
+    new = gather(main, g, cn, ck)
+    got = new - gather(main0, g, cn, ck)
+    tol = REL_TOL * np.linalg.norm(want) + 2.0 ** -24 * np.abs(new).max() * np.sqrt(n_s)
+    assert np.linalg.norm(got - want) <= tol, "wgrad (sampled, accumulate)"
+    for e in np.flatnonzero(w.splits == 0):
+        assert torch.equal(main[e], main0[e]), f"empty expert {e} changed"

@@ -260,3 +260,28 @@ def test_gemms_on_exact_operands_equal_matmul():
         assert np.allclose(dwa[g], init[g] + dy[a:b].T @ x[a:b], rtol=1e-15, atol=0)
     assert np.all(dw[1] == 0)
     assert np.all(np.isnan(y[L:])) and np.all(np.isnan(dx[L:]))
+
+
+def test_sampled_gemms_equal_the_full_gemms():
+    """The one-dot-product-per-sample oracle (used at full size) against the
+    pinned full GEMMs, at every sampled position, all three kinds."""
+    splits = np.array([96, 0, 32, 160], np.int32)
+    G, N, K, pad = 4, 256, 256, 32
+    L = int(splits.sum())
+    x = np.concatenate([W.normal_bf16((L, K), 25), W.uniform_bf16((pad, K), 26, -4, 4)])
+    dy = np.concatenate([W.normal_bf16((L, N), 27), W.uniform_bf16((pad, N), 28, -4, 4)])
+    w = W.normal_bf16((G * N, K), 29, scale=0.02)
+    xq, dq, wq = O.quantize_nvfp4(x, splits, G), O.quantize_nvfp4(dy, splits, G), O.quantize_nvfp4(w, None, G)
+    rng = np.random.default_rng(30)
+    rows = rng.integers(0, L, 300)
+    cn, ck = rng.integers(0, N, 300), rng.integers(0, K, 300)
+    g = rng.choice(np.flatnonzero(splits > 0), 300)
+    y = O.gemm_nvfp4("fprop", xq, wq, splits, G, N, K)
+    dx = O.gemm_nvfp4("dgrad", dq, wq, splits, G, N, K)
+    dw = O.gemm_nvfp4("wgrad", dq, xq, splits, G, N, K)
+    np.testing.assert_allclose(O.gemm_nvfp4_sample("fprop", xq, wq, splits, G, N, K, rows, cn), y[rows, cn],
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(O.gemm_nvfp4_sample("dgrad", dq, wq, splits, G, N, K, rows, ck), dx[rows, ck],
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(O.gemm_nvfp4_sample("wgrad", dq, xq, splits, G, N, K, cn, ck, g), dw[g, cn, ck],
+                               rtol=1e-12, atol=1e-12)
