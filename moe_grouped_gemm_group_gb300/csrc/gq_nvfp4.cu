@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(256) k_nv_amax(const uint16_t* __restrict__ x,
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const uint4* src = reinterpret_cast<const uint4*>(x + 32 * blk * cols);
         uint32_t mx = 0;
-#pragma unroll 4
+#pragma unroll 8
         for (int64_t i = tid; i < chunks; i += 256) {
             const uint4 v = __ldg(src + i);
             mx = max(mx, max(max(v.x & 0x7fffu, v.x >> 16 & 0x7fffu), max(v.y & 0x7fffu, v.y >> 16 & 0x7fffu)));
@@ -256,14 +256,19 @@ __global__ void __launch_bounds__(256) k_nv_amax(const uint16_t* __restrict__ x,
 // Shared-memory plan of k_nv_quant: a ring of kNqStages bf16 input tiles
 // (128 rows x 128 columns, two 128-byte-swizzled TMA boxes of [128 rows][64
 // columns]) with the tile's table m[sf]; two output staging buffers (the
-// columnwise codes [128 columns][64 bytes] and the tile's four atoms); the
-// ring's barriers; the split scan.
+// columnwise codes and the tile's four atoms); the ring's barriers; the
+// split scan.
 constexpr int kNqStages = 5;
 constexpr int kNqTile = 128 * 128 * 2;
 constexpr int kNqConsumers = 512;                     // 16 consumer warps
 constexpr int kNqThreads = kNqConsumers + 32;         // + 1 producer warp
-constexpr int kNqOut = 128 * 64 + 4 * 512;
-constexpr int kNqSmem = 1024 + kNqStages * kNqTile + kNqStages * 512 + 2 * kNqOut + 2 * 8 * kNqStages + 16 + kScanBytes;
+// columnwise code staging: [16-row block b][column c] x 8 bytes, rows of
+// 1056 bytes (1024 + 32 of padding: the read-out's column groups of
+// different blocks then fall on different banks)
+constexpr int kNqStagePitch = 1024 + 32;
+constexpr int kNqOut = 8 * kNqStagePitch + 4 * 512;
+constexpr int kNqSmem = 1024 + kNqStages * kNqTile + kNqStages * 512 + 2 * kNqOut + kNqStages * 32 +
+                        2 * 8 * kNqStages + 16 + kScanBytes;
 
 // Tile order of the quantiser (tuning knob): tiles are walked in bands of
 // GQ_NQ_BAND row tiles, row tile fastest inside a band, so that the CTAs
@@ -276,13 +281,15 @@ constexpr int kNqSmem = 1024 + kNqStages * kNqTile + kNqStages * 512 + 2 * kNqOu
 constexpr int kNqBand = GQ_NQ_BAND;
 
 // One 128 x 128 tile of one group (the group's own 128-row tiles, so one S_g
-// per tile).
+// per tile).  32 bytes: the producer decodes each tile once and hands it to
+// the consumers with the stage.
 struct NqTile {
     int g;
     int rows;          // live rows (a multiple of 32)
     int64_t mt, ct;    // row tile in the group, column tile
     int64_t row0;      // first buffer row
 };
+static_assert(sizeof(NqTile) == 32, "tile record size");
 
 __device__ __forceinline__ NqTile nq_tile(const Scan& sc, int G, int64_t nct, int64_t t)
 {
@@ -327,7 +334,8 @@ k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ C
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* mtabs = reinterpret_cast<float*>(tiles + kNqStages * kNqTile);     // [stage][128]
     uint8_t* outs = reinterpret_cast<uint8_t*>(mtabs + kNqStages * 128);     // [2][ccodes | atoms]
-    uint64_t* full = reinterpret_cast<uint64_t*>(outs + 2 * kNqOut);
+    NqTile* infos = reinterpret_cast<NqTile*>(outs + 2 * kNqOut);            // [stage]
+    uint64_t* full = reinterpret_cast<uint64_t*>(infos + kNqStages);
     uint64_t* empty = full + kNqStages;
     volatile int* abort = reinterpret_cast<volatile int*>(empty + kNqStages);
     if (load_status(status) != 0)
@@ -365,6 +373,8 @@ k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ C
             // entry 127 (an E4M3 NaN byte, never a scale) carries S_g itself
             for (int e = lane; e < 128; e += 32)
                 mtabs[s * 128 + e] = e == 127 ? S : nv_encode_mult(S, (uint32_t)e);
+            if (lane == 0)
+                infos[s] = q;
             __syncwarp();
             if (lane == 0) {
                 uint8_t* dst = tiles + s * kNqTile;
@@ -403,16 +413,20 @@ k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ C
         const bool ok = ptx::mbar_wait_warp(&full[s], ph, abort, status);
         if (ptx::named_barrier_or(1, kNqConsumers, !ok))
             break;
-        const NqTile q = nq_tile(sc, G, nct, t);
+        const NqTile q = infos[s];
         const int rows = q.rows;
         const uint32_t tile = ptx::smem_addr(tiles + s * kNqTile);
         const float* mtab = mtabs + s * 128;
         const float S = mtab[127];
         uint8_t* ccodes = outs + ob * kNqOut;
-        uint8_t* atoms = ccodes + 128 * 64;
+        uint8_t* atoms = ccodes + 8 * kNqStagePitch;
         if (ROW) {
             for (int i = tid; i < 128 * 8; i += kNqConsumers) {
-                const int r = i >> 3, jb = i & 7;       // row, 16-column block
+                // row r, 16-column block jb: a warp takes 8 consecutive rows x 4
+                // blocks, so each quarter-warp's 16-byte reads hit 8 different
+                // swizzled chunks (no bank conflict)
+                const int w = i >> 5, l = i & 31;
+                const int r = (w & 15) * 8 + (l & 7), jb = (w >> 4) * 4 + (l >> 3);
                 uint32_t sf = 0;
                 if (r < rows) {
                     const int h = jb >> 2, j = 2 * (jb & 3);
@@ -447,8 +461,7 @@ k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ C
                 uint2 c0, c1;
                 sf0 = nv_encode16_t(v0, __uint_as_float((m & 0xffffu) << 16), S, mtab, c0);
                 sf1 = nv_encode16_t(v1, __uint_as_float(m & 0xffff0000u), S, mtab, c1);
-                *reinterpret_cast<uint2*>(ccodes + (2 * p) * 64 + b * 8) = c0;
-                *reinterpret_cast<uint2*>(ccodes + (2 * p + 1) * 64 + b * 8) = c1;
+                *reinterpret_cast<uint4*>(ccodes + b * kNqStagePitch + 16 * p) = make_uint4(c0.x, c0.y, c1.x, c1.y);
             }
             const int c = 2 * p;
             atoms[(2 + (b >> 2)) * 512 + (c & 31) * 16 + (c >> 5) * 4 + (b & 3)] = (uint8_t)sf0;
@@ -465,9 +478,11 @@ k_nv_quant(const __grid_constant__ CUtensorMap map128, const __grid_constant__ C
             const int64_t T = sc.tp[q.g + 1] - sc.tp[q.g];
             const int nch = rows / 32;                 // 16-byte chunks of a column (rows / 2 bytes)
             for (int i = tid; i < 128 * nch; i += kNqConsumers) {
-                const int c = i / nch, ch = i - c * nch;
+                const int c = i / nch, ch = i - c * nch;  // chunk ch = blocks 2 ch, 2 ch + 1
+                const uint2 lo = *reinterpret_cast<const uint2*>(ccodes + (2 * ch) * kNqStagePitch + 8 * c);
+                const uint2 hi = *reinterpret_cast<const uint2*>(ccodes + (2 * ch + 1) * kNqStagePitch + 8 * c);
                 *reinterpret_cast<uint4*>(col_data + (q.ct * 128 + c) * (rows_cap / 2) + q.row0 / 2 + ch * 16) =
-                    *reinterpret_cast<const uint4*>(ccodes + c * 64 + ch * 16);
+                    make_uint4(lo.x, lo.y, hi.x, hi.y);
             }
             if (tid >= 64 && tid < 128)
                 *reinterpret_cast<uint4*>(col_scale + sb + (q.ct * 2 * T + 2 * q.mt) * 512 + (tid - 64) * 16) =
