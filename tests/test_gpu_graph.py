@@ -3,7 +3,8 @@ dgrad and wgrad (accumulating into fp32 main grads), every quantisation
 included, with the split sizes on the device.  The step is captured once and
 replayed with new split sizes and new inputs written into the same buffers;
 each replay must give, bit for bit, what eager calls give on the same
-inputs (TransformerEngine PR 3224: device split sizes, no host sync)."""
+inputs (TransformerEngine PR 3224: device split sizes, no host sync).  Both
+the MXFP8 and the NVFP4 recipe."""
 import numpy as np
 import pytest
 
@@ -21,8 +22,8 @@ SPLITS = [np.array([256, 0, 416, 288], np.int32), np.array([96, 512, 32, 320], n
 
 
 class Layer:
-    def __init__(self):
-        mx = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    def __init__(self, kind=gq.RECIPE_MXFP8_1X32):
+        mx = gq.Recipe(kind, 1, 1, 0.0)
         self.mx = mx
         bf = torch.bfloat16
         self.inp = {"x1": torch.empty((R, H), dtype=bf, device=DEV), "x2": torch.empty((R, F), dtype=bf, device=DEV),
@@ -76,8 +77,9 @@ def _same_bits(a, b):
     return torch.equal(ia, ib)
 
 
-def test_captured_step_replays_like_eager_calls():
-    layer = Layer()
+@pytest.mark.parametrize("kind", [gq.RECIPE_MXFP8_1X32, gq.RECIPE_NVFP4_1X16])
+def test_captured_step_replays_like_eager_calls(kind):
+    layer = Layer(kind)
     layer.load(0, SPLITS[0])
     layer.step()                          # first calls on the device: set-up outside capture
     layer.results()
