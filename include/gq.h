@@ -172,7 +172,8 @@ uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64
  *   d_table[g]                     = o_g, the first row of group g (g = G: L)
  *   d_table[(G + 1) + g]           = T_0 + ... + T_{g-1}, T_h = ceil(m_h / 128)
  *   d_table[2 (G + 1) + g]         = byte offset of group g's scale region
- *                                    (MX: 512 (cols/128) sum T; per-channel:
+ *                                    (MX: 512 (cols/128) sum T; NVFP4:
+ *                                    512 (cols/64) sum T; per-channel:
  *                                    4 cols o_g / 128)
  * Split errors go to *d_status and leave d_table untouched.  Every other
  * call performs this scan inside its own kernels; this entry point exposes

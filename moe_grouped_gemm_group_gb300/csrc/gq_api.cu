@@ -192,12 +192,13 @@ gq_status gq_split_scan(const int32_t* d_split_sizes, int32_t num_groups, int64_
 {
     if (!d_table || !d_status)
         return GQ_ERR_INVALID_ARG;
-    if (recipe_kind != GQ_RECIPE_MXFP8_1X32 && recipe_kind != GQ_RECIPE_CHANNEL128_F32)
+    if (recipe_kind != GQ_RECIPE_MXFP8_1X32 && recipe_kind != GQ_RECIPE_CHANNEL128_F32 &&
+        recipe_kind != GQ_RECIPE_NVFP4_1X16)
         return GQ_ERR_UNSUPPORTED;
     gq_status st = check_partition(d_split_sizes, num_groups, rows_cap, cols);
     if (st != GQ_OK)
         return st;
-    const int align = recipe_kind == GQ_RECIPE_MXFP8_1X32 ? 32 : 128;
+    const int align = recipe_kind == GQ_RECIPE_CHANNEL128_F32 ? 128 : 32;
     return cuda_status(gq::launch_split_scan(d_split_sizes, num_groups, rows_cap, cols, align,
                                              recipe_kind, d_table, d_status,
                                              (cudaStream_t)stream));

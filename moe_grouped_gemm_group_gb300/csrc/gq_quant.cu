@@ -120,8 +120,9 @@ __global__ void k_split_scan(const int32_t* __restrict__ splits, int G, int64_t 
     for (int g = threadIdx.x; g <= G; g += blockDim.x) {
         table[g] = s_off[g];
         table[G + 1 + g] = s_tp[g];
-        table[2 * (G + 1) + g] = scale_kind == 0 ? 512 * (cols >> 7) * (int64_t)s_tp[g]
-                                                 : 4 * cols * (s_off[g] >> 7);
+        table[2 * (G + 1) + g] = scale_kind == 0   ? 512 * (cols >> 7) * (int64_t)s_tp[g]
+                                 : scale_kind == 2 ? 512 * (cols >> 6) * (int64_t)s_tp[g]
+                                                   : 4 * cols * (s_off[g] >> 7);
     }
 }
 

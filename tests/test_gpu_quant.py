@@ -157,6 +157,16 @@ def test_split_scan_table():
                      gq.RECIPE_CHANNEL128_F32, table, st)
     off, tp, sb = O.split_scan(np.array([128, 256], np.int32), 2, 512, 384, O.RECIPE_CHANNEL)
     np.testing.assert_array_equal(host(table)[:9], np.concatenate([off, tp, sb]))
+    # NVFP4: the same partition, scale regions of 512 (cols/64) bytes per 128-row tile,
+    # the last entry being the bytes the oracle's quantiser fills
+    table.zero_()
+    gq.gq_split_scan(splits_dev(splits), G, 512, 384, gq.RECIPE_NVFP4_1X16, table, st)
+    check_status(st)
+    off, tp, _ = O.split_scan(splits, G, 512, 384)
+    got = host(table)
+    np.testing.assert_array_equal(got[:2 * (G + 1)], np.concatenate([off, tp]))
+    np.testing.assert_array_equal(got[2 * (G + 1):], 512 * (384 // 64) * tp)
+    assert got[-1] == O.scale_bytes_nvfp4(splits, G, 512, 384)
     gq.gq_split_scan(splits_dev(np.array([128, 48], np.int32)), 2, 512, 384,
                      gq.RECIPE_MXFP8_1X32, table, st)
     check_status(st, -3)
