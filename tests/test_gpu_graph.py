@@ -102,3 +102,71 @@ def test_captured_step_replays_like_eager_calls(kind):
         # the live rows were written; the rows past the live total were not
         assert not torch.isnan(got["y1"][:L].float()).any()
         assert torch.isnan(got["y1"][L:].float()).all()
+
+
+@pytest.mark.parametrize("kind", [gq.RECIPE_MXFP8_1X32, gq.RECIPE_NVFP4_1X16])
+def test_weight_cache_reused_across_microbatches_in_a_graph(kind):
+    """The weights are quantised once into a preallocated descriptor (the
+    output reuse of TransformerEngine PR 3224's group_quantize) and that cache
+    serves three microbatches, each with its own device split sizes and
+    inputs: fprop, dgrad and a wgrad accumulating into one fp32 main grad.
+    The whole sequence is captured once; replays give the eager bits."""
+    rec = gq.Recipe(kind, 1, 1, 0.0)
+    bf = torch.bfloat16
+    nmb = 3
+    w = torch.empty((G * F, H), dtype=bf, device=DEV)
+    qw = gq.alloc_quantized(G * F, H, G, rec, DEV)
+    xs = [torch.empty((R, H), dtype=bf, device=DEV) for _ in range(nmb)]
+    dys = [torch.empty((R, F), dtype=bf, device=DEV) for _ in range(nmb)]
+    sps = [torch.zeros(G, dtype=torch.int32, device=DEV) for _ in range(nmb)]
+    qx = [gq.alloc_quantized(R, H, G, rec, DEV) for _ in range(nmb)]
+    qd = [gq.alloc_quantized(R, F, G, rec, DEV) for _ in range(nmb)]
+    ys = [torch.empty((R, F), dtype=bf, device=DEV) for _ in range(nmb)]
+    dxs = [torch.empty((R, H), dtype=bf, device=DEV) for _ in range(nmb)]
+    dw = torch.empty((G, F, H), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=DEV)
+
+    def load(seed):
+        gen = torch.Generator(device=DEV).manual_seed(seed)
+        w.copy_(torch.randn(w.shape, generator=gen, device=DEV) * 0.02)
+        dw.copy_(torch.randn(dw.shape, generator=gen, device=DEV) * 1e-3)
+        for m in range(nmb):
+            xs[m].copy_(torch.randn(xs[m].shape, generator=gen, device=DEV))
+            dys[m].copy_(torch.randn(dys[m].shape, generator=gen, device=DEV))
+            sps[m].copy_(torch.from_numpy(SPLITS[(seed + m) % 2]))
+            ys[m].fill_(float("nan"))
+            dxs[m].fill_(float("nan"))
+
+    def run():
+        gq.gq_quantize(w, None, G, rec, qw, st)              # once per step: the weight cache
+        for m in range(nmb):
+            gq.gq_quantize(xs[m], sps[m], G, rec, qx[m], st)
+            gq.gq_quantize(dys[m], sps[m], G, rec, qd[m], st)
+            gq.gq_gemm_fprop(qx[m], qw, sps[m], G, F, H, ys[m], gq.DTYPE_BF16, st)
+            gq.gq_gemm_dgrad(qd[m], qw, sps[m], G, F, H, dxs[m], gq.DTYPE_BF16, st)
+            gq.gq_gemm_wgrad(qd[m], qx[m], sps[m], G, F, H, dw, True, st, workspace=ws)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        check_status(st)
+        return [t.clone() for t in ys + dxs + [dw]]
+
+    load(0)
+    run()
+    snapshot()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for seed in (1, 2):
+        load(seed)
+        graph.replay()
+        got = snapshot()
+        load(seed)
+        run()
+        want = snapshot()
+        for m in range(nmb):
+            L = int(SPLITS[(seed + m) % 2].sum())
+            assert _same_bits(got[m][:L], want[m][:L]), f"seed {seed}: y of microbatch {m}"
+            assert _same_bits(got[nmb + m][:L], want[nmb + m][:L]), f"seed {seed}: dx of microbatch {m}"
+        assert _same_bits(got[-1], want[-1]), f"seed {seed}: accumulated dW"
