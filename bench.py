@@ -272,10 +272,14 @@ class Step:
         self.cdw = torch.empty((4, cw.hidden, cw.ffn), dtype=torch.float32, device=device)
         self._build_launches()
 
-    def _build_launches(self):
+    def _build_launches(self, sp=None, csp=None):
+        """The step's launches reading split sizes from `sp` / `csp` (default:
+        the device-timed step's buffers); sets self.launches and returns it."""
         gq, q, o, i = self.gq, self.q, self.out, self.inputs
         E, H, F, L = self.E, self.H, self.F, self.L
-        sp, st, mx = self.splits, self.status, self.mx
+        sp = self.splits if sp is None else sp
+        csp = self.csplits if csp is None else csp
+        st, mx = self.status, self.mx
         live_groups = int(np.count_nonzero(self.wl.splits))
         cw = self.cw
         cl = int(cw.live_rows)
@@ -302,15 +306,16 @@ class Step:
             ("wgrad1", "g", lambda: gq.gq_gemm_wgrad(q["dy1"], q["x1"], sp, E, F, H, o["dw1"], True, st,
                                                      workspace=self.ws),
              (2.0 * L * F * H, L * (H + F) * (1 + 1 / 32) + live_groups * F * H * 8.0)),
-            ("quant_ch_dy", "q", lambda: gq.gq_quantize(self.cin["dy"], self.csplits, 4, self.ch,
+            ("quant_ch_dy", "q", lambda: gq.gq_quantize(self.cin["dy"], csp, 4, self.ch,
                                                          self.cq["dy"], st), (3 + 4 / 128) * cl * cw.hidden),
-            ("quant_ch_x", "q", lambda: gq.gq_quantize(self.cin["x"], self.csplits, 4, self.ch,
+            ("quant_ch_x", "q", lambda: gq.gq_quantize(self.cin["x"], csp, 4, self.ch,
                                                         self.cq["x"], st), (3 + 4 / 128) * cl * cw.ffn),
-            ("wgrad_ch", "g", lambda: gq.gq_gemm_wgrad(self.cq["dy"], self.cq["x"], self.csplits, 4,
+            ("wgrad_ch", "g", lambda: gq.gq_gemm_wgrad(self.cq["dy"], self.cq["x"], csp, 4,
                                                        cw.hidden, cw.ffn, self.cdw, False, st),
              (2.0 * cl * cw.hidden * cw.ffn, cl * (cw.hidden + cw.ffn) + 4 * cw.hidden * cw.ffn * 4.0)),
         ]
         self.gemm_flops = sum(u[0] for _, k, _, u in self.launches if k == "g")
+        return self.launches
 
     def run(self, events=None):
         """One step; with `events`, bracket every launch with CUDA events."""
@@ -349,6 +354,13 @@ class Step:
         self.s_down = torch.cuda.Stream()
         self.ev_used = {}       # input -> its last use in the previous step
         self.ev_read = {}       # output -> its copy to the host in the previous step
+        # e2e steps alternate between two device copies of the split sizes,
+        # each with its own launch list, so that a step's split upload only
+        # waits for the step before the previous one
+        self.e2e_sp = [(self.splits, self.csplits), (self.splits.clone(), self.csplits.clone())]
+        self.e2e_launches = [self._build_launches(*b) for b in self.e2e_sp]
+        self.launches = self.e2e_launches[0]
+        self.e2e_iter = 0
 
     # Which buffers each launch reads from the host's inputs and which of the
     # copied-back results it writes.
@@ -371,11 +383,22 @@ class Step:
         rewrites a result waits for the previous step's download of it."""
         torch = self.torch
         cur = torch.cuda.current_stream()
-        self.splits.copy_(self.h_splits, non_blocking=True)
-        self.csplits.copy_(self.h_csplits, non_blocking=True)
+        par = self.e2e_iter & 1
+        self.e2e_iter += 1
+        launches = self.e2e_launches[par]
+        sp, csp = self.e2e_sp[par]
         ready = {}
         with torch.cuda.stream(self.s_up):
-            for name, _, _, _ in self.launches:
+            # the split sizes first, on the upload stream: a copy issued on the
+            # compute stream would queue behind the step's large uploads in
+            # the copy engine and hold every launch until all inputs are in
+            if ("splits", par) in self.ev_used:
+                self.s_up.wait_event(self.ev_used[("splits", par)])
+            sp.copy_(self.h_splits, non_blocking=True)
+            csp.copy_(self.h_csplits, non_blocking=True)
+            splits_ready = torch.cuda.Event()
+            splits_ready.record(self.s_up)
+            for name, _, _, _ in launches:
                 for k in self.E2E_INPUTS.get(name, ()):
                     if k in self.ev_used:
                         self.s_up.wait_event(self.ev_used[k])
@@ -383,7 +406,8 @@ class Step:
                     ready[k] = torch.cuda.Event()
                     ready[k].record(self.s_up)
         produced = []
-        for name, _, fn, _ in self.launches:
+        cur.wait_event(splits_ready)
+        for name, _, fn, _ in launches:
             for k in self.E2E_INPUTS.get(name, ()):
                 cur.wait_event(ready[k])
             for o in self.E2E_OUTPUTS.get(name, ()):
@@ -398,6 +422,7 @@ class Step:
                 produced.append((o, done))
         last = torch.cuda.Event()
         last.record(cur)
+        self.ev_used[("splits", par)] = last      # the step's last reader of these split sizes
         with torch.cuda.stream(self.s_down):
             for o, ev in produced:
                 self.s_down.wait_event(ev)
