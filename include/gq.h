@@ -77,9 +77,9 @@ typedef enum gq_recipe_kind {
      * codes = e4m3(x * (1 / sf)). */
     GQ_RECIPE_CHANNEL128_F32 = 1,
     /* NVFP4: FP4 E2M1 codes with one E4M3 scale per 16 elements along the
-     * contraction axis and one fp32 second-level scale per group.  The pages
-     * name NVFP4 beside MXFP8 on the grouped paths (TransformerEngine PR
-     * 3224) without defining it; this is the public NVFP4 format.  Per group
+     * contraction axis and one fp32 second-level scale per group.
+     * TransformerEngine PR 3224 names NVFP4 beside MXFP8 on the grouped paths
+     * without defining it; this is the public NVFP4 format.  Per group
      * g: amax_g = max |x| over its live rows, S_g = 2688 / amax_g (1 when
      * amax_g == 0, clamped to FLT_MAX).  Per block, in fp32 op by op:
      * s = (amax_b / 6) * S_g, sf = e4m3(s) (nearest-even, saturating),

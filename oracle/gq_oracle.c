@@ -785,9 +785,9 @@ int or_srelu_quantize_mx(const float* y, const float* probs, int64_t rows_cap, i
 /* second-level scale per group                                              */
 /* ------------------------------------------------------------------------ */
 /*
- * The pages name NVFP4 as a second quantiser on the same grouped code paths
- * (TransformerEngine PR 3224, the NVFP4 note beside the MXFP8 changes)
- * without defining it.  Reading taken: the public NVFP4 format.
+ * TransformerEngine PR 3224 names NVFP4 as a second quantiser on the same
+ * grouped code paths (its NVFP4 note beside the MXFP8 changes) without
+ * defining it.  Reading taken: the public NVFP4 format.
  *  - Codes are FP4 E2M1 (values +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}); conversion
  *    rounds to nearest, ties to even, saturates to +-6, and a value that
  *    rounds to zero keeps its sign.  Two codes per byte, the element with the

@@ -1,9 +1,9 @@
 """Pins of the oracle's NVFP4 recipe (E2M1 codes, 16-element blocks with E4M3
 scales, one fp32 second-level scale per group) and of its grouped GEMMs.
 
-The pages name NVFP4 as a second quantiser of the same grouped paths
-(TransformerEngine PR 3224) without defining it; the oracle follows the
-public NVFP4 format (the reading is written out in gq_oracle.c).  The pins
+TransformerEngine PR 3224 names NVFP4 as a second quantiser of the same
+grouped paths without defining it; the oracle follows the public NVFP4
+format (the reading is written out in gq_oracle.c).  The pins
 do not restate its arithmetic:
   * the E2M1 value table of the format, and a brute-force nearest-even
     search over it;
