@@ -3,7 +3,7 @@
 size, the tile-to-group search over it, and the wgrad's in-CTA sort of the
 groups by size for its run-time tile order.  Quantisation bitwise against
 the oracle; fprop (128-column tiles), dgrad and wgrad (256-column tiles, both
-tile orders) at the GEMMs' tolerance."""
+tile orders) at the GEMMs' tolerance; the same for the NVFP4 recipe."""
 import numpy as np
 import pytest
 
@@ -91,3 +91,50 @@ def test_gemms_1024_groups(data):
         else:
             e = np.linalg.norm(got[g].astype(np.float64) - want[g]) / np.linalg.norm(want[g])
             assert e <= REL_TOL, f"wgrad group {g}: rel err {e}"
+
+
+def test_nvfp4_1024_groups(data):
+    """The NVFP4 recipe at the maximum group count: per-group amax, codes and
+    scales bitwise; fprop, dgrad and wgrad (the last 64-row block of every
+    32-row group half live) at the GEMMs' tolerance."""
+    splits, L, R, x, _, _ = data
+    N = 256                                  # NVFP4 GEMMs take n, k multiples of 256
+    dy = np.concatenate([W.normal_bf16((L, N), 97), W.uniform_bf16((R - L, N), 98, -4, 4)])
+    w = W.normal_bf16((G * N, K), 99, scale=0.05)
+    off = np.concatenate([[0], np.cumsum(splits)])
+    bounds = [(int(off[g]), int(off[g + 1])) for g in range(G)]
+    nv = gq.Recipe(gq.RECIPE_NVFP4_1X16, 1, 1, 0.0)
+    st = status_dev()
+
+    def q(bits, sp):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+        out = gq.alloc_quantized(t.shape[0], t.shape[1], G, nv, DEV)
+        gq.gq_quantize(t, splits_dev(sp), G, nv, out, st)
+        return out
+
+    xq, dq, wq = q(x, splits), q(dy, splits), q(w, None)
+    sp = splits_dev(splits)
+    y = torch.empty((R, N), device=DEV)
+    dx = torch.empty((R, K), device=DEV)
+    dw = torch.full((G, N, K), float("nan"), device=DEV)
+    gq.gq_gemm_fprop(xq, wq, sp, G, N, K, y, gq.DTYPE_F32, st)
+    gq.gq_gemm_dgrad(dq, wq, sp, G, N, K, dx, gq.DTYPE_F32, st)
+    gq.gq_gemm_wgrad(dq, xq, sp, G, N, K, dw, False, st)
+    check_status(st)
+    ox, ody, ow = O.quantize_nvfp4(x, splits, G), O.quantize_nvfp4(dy, splits, G), O.quantize_nvfp4(w, None, G)
+    assert np.array_equal(host(xq.amax)[:G], ox.amax)
+    assert np.array_equal(host(xq.row_data)[:L], ox.row_data[:L])
+    assert np.array_equal(host(xq.col_data)[:, :L // 2], ox.col_data[:, :L // 2])
+    nb = O.scale_bytes_nvfp4(splits, G, R, K)
+    assert np.array_equal(host(xq.row_scale)[:nb], ox.row_scale[:nb])
+    assert np.array_equal(host(xq.col_scale)[:nb], ox.col_scale[:nb])
+    _close_groups(host(y), O.gemm_nvfp4("fprop", ox, ow, splits, G, N, K), bounds, "nvfp4 fprop")
+    _close_groups(host(dx), O.gemm_nvfp4("dgrad", ody, ow, splits, G, N, K), bounds, "nvfp4 dgrad")
+    want = O.gemm_nvfp4("wgrad", ody, ox, splits, G, N, K)
+    got = host(dw)
+    for g in range(G):
+        if splits[g] == 0:
+            assert np.all(got[g] == 0), f"group {g} is empty"
+        else:
+            e = np.linalg.norm(got[g].astype(np.float64) - want[g]) / np.linalg.norm(want[g])
+            assert e <= REL_TOL, f"nvfp4 wgrad group {g}: rel err {e}"
