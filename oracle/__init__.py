@@ -92,6 +92,14 @@ def _load():
                                               C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
             lib.or_gemm_nvfp4.argtypes = ([C.c_int] + [C.c_void_p] * 7 +
                                           [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int, C.c_void_p])
+            lib.or_act_exp.restype = C.c_float
+            lib.or_act_exp.argtypes = [C.c_float]
+            lib.or_act_silu.restype = C.c_float
+            lib.or_act_silu.argtypes = [C.c_float]
+            lib.or_swiglu_quantize_mx.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                                  C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p,
+                                                  C.c_void_p, C.c_int64]
+            lib.or_swiglu_quantize_mx.restype = C.c_int
             lib.or_gemm_nvfp4_sample.argtypes = ([C.c_int] + [C.c_void_p] * 7 +
                                                  [C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p])
@@ -226,6 +234,37 @@ def srelu_quantize_mx(y: np.ndarray, probs: np.ndarray, splits, num_groups: int,
     st = lib.or_srelu_quantize_mx(_p(yy), _p(pr), R, Cc, _p(s), num_groups, _p(rd), _p(rs), need, _p(cd),
                                   _p(cs), need)
     _check(st, "srelu_quantize_mx")
+    return MXQuantized(rd, rs, cd, cs, s, R, Cc)
+
+
+def act_exp(x: float) -> float:
+    """The activation's own exp (fp32; see or_act_exp)."""
+    return float(_load().or_act_exp(float(x)))
+
+
+def act_silu(x: float) -> float:
+    return float(_load().or_act_silu(float(x)))
+
+
+def swiglu_quantize_mx(y: np.ndarray, probs: np.ndarray, splits, num_groups: int, data_fill: int = 0,
+                       scale_fill: int = 0) -> MXQuantized:
+    """ScaledSwiGLU of an fp32 [R, 2C] buffer (gate half, then linear half),
+    a = (silu(gate) * linear) * probs[r] in fp32, then MXFP8 1x32 quantisation
+    of the [R, C] activation rowwise and columnwise (as quantize_mx)."""
+    lib = _load()
+    yy = np.ascontiguousarray(y, np.float32)
+    pr = np.ascontiguousarray(probs, np.float32)
+    R, C2 = yy.shape
+    Cc = C2 // 2
+    s = _splits(splits)
+    need = int(split_scan(s, num_groups, R, Cc)[2][-1])
+    rd = np.full((R, Cc), data_fill, np.uint8)
+    cd = np.full((R, Cc), data_fill, np.uint8)
+    rs = np.full(max(need, 1), scale_fill, np.uint8)
+    cs = np.full(max(need, 1), scale_fill, np.uint8)
+    st = lib.or_swiglu_quantize_mx(_p(yy), _p(pr), R, Cc, _p(s), num_groups, _p(rd), _p(rs), need, _p(cd),
+                                   _p(cs), need)
+    _check(st, "swiglu_quantize_mx")
     return MXQuantized(rd, rs, cd, cs, s, R, Cc)
 
 

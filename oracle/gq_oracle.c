@@ -697,6 +697,51 @@ int or_grouped_bias_grad(const uint16_t* dy, const int32_t* splits, int G, int64
 /* ScaledSReLU + MXFP8 quantisation of an fp32 activation                    */
 /* ------------------------------------------------------------------------ */
 
+/* MXFP8 1x32 quantisation of an fp32 [L, cols] array `a` (the live rows of
+ * a grouped buffer), rowwise and columnwise, with the scale rule, codes and
+ * swizzled layout of or_quantize_mx; the scale regions are zeroed first. */
+static void mx_quantize_f32(const float* a, int64_t cols, const int64_t* off, const int64_t* tp,
+                            const int64_t* sb, int G, uint8_t* row_data, uint8_t* row_scale,
+                            uint8_t* col_data, uint8_t* col_scale)
+{
+    memset(row_scale, 0, (size_t)sb[G]);
+    memset(col_scale, 0, (size_t)sb[G]);
+    for (int g = 0; g < G; ++g) {
+        int64_t o = off[g], m = off[g + 1] - off[g], T = tp[g + 1] - tp[g];
+#pragma omp parallel for schedule(static)
+        for (int64_t lr = 0; lr < m; ++lr) {
+            int64_t r = o + lr;
+            for (int64_t j = 0; j < cols / 32; ++j) {
+                double amax = 0.0;
+                int e;
+                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
+                    if (fabs((double)a[r * cols + c]) > amax)
+                        amax = fabs((double)a[r * cols + c]);
+                e = or_mx_scale_exponent(amax);
+                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
+                    row_data[r * cols + c] = or_e4m3_encode(ldexp((double)a[r * cols + c], -e));
+                row_scale[sb[g] + ((lr / 128) * (cols / 128) + j / 4) * 512 + atom_byte(lr % 128, j % 4)] =
+                    (uint8_t)(e + 127);
+            }
+        }
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; ++c) {
+            for (int64_t b = 0; b < m / 32; ++b) {
+                double amax = 0.0;
+                int e;
+                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
+                    if (fabs((double)a[(o + lr) * cols + c]) > amax)
+                        amax = fabs((double)a[(o + lr) * cols + c]);
+                e = or_mx_scale_exponent(amax);
+                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
+                    col_data[(o + lr) * cols + c] = or_e4m3_encode(ldexp((double)a[(o + lr) * cols + c], -e));
+                col_scale[sb[g] + ((c / 128) * T + b / 4) * 512 + atom_byte(c % 128, b % 4)] = (uint8_t)(e + 127);
+            }
+        }
+    }
+}
+
+
 /* a = probs[r] * relu(y)^2 in fp32, op by op: t = max(y, 0); t = t * t;
  * a = t * probs[r] (the ScaledSReLU between fc1 and fc2 in TransformerEngine
  * issue 3484's reproducer, te.ops.ScaledSReLU, fed with per-token probs;
@@ -740,41 +785,7 @@ int or_srelu_quantize_mx(const float* y, const float* probs, int64_t rows_cap, i
             t = t * t;
             a[r * cols + c] = t * probs[r];
         }
-    memset(row_scale, 0, (size_t)sb[G]);
-    memset(col_scale, 0, (size_t)sb[G]);
-    for (int g = 0; g < G; ++g) {
-        int64_t o = off[g], m = off[g + 1] - off[g], T = tp[g + 1] - tp[g];
-#pragma omp parallel for schedule(static)
-        for (int64_t lr = 0; lr < m; ++lr) {
-            int64_t r = o + lr;
-            for (int64_t j = 0; j < cols / 32; ++j) {
-                double amax = 0.0;
-                int e;
-                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
-                    if (fabs((double)a[r * cols + c]) > amax)
-                        amax = fabs((double)a[r * cols + c]);
-                e = or_mx_scale_exponent(amax);
-                for (int64_t c = 32 * j; c < 32 * j + 32; ++c)
-                    row_data[r * cols + c] = or_e4m3_encode(ldexp((double)a[r * cols + c], -e));
-                row_scale[sb[g] + ((lr / 128) * (cols / 128) + j / 4) * 512 + atom_byte(lr % 128, j % 4)] =
-                    (uint8_t)(e + 127);
-            }
-        }
-#pragma omp parallel for schedule(static)
-        for (int64_t c = 0; c < cols; ++c) {
-            for (int64_t b = 0; b < m / 32; ++b) {
-                double amax = 0.0;
-                int e;
-                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
-                    if (fabs((double)a[(o + lr) * cols + c]) > amax)
-                        amax = fabs((double)a[(o + lr) * cols + c]);
-                e = or_mx_scale_exponent(amax);
-                for (int64_t lr = 32 * b; lr < 32 * b + 32; ++lr)
-                    col_data[(o + lr) * cols + c] = or_e4m3_encode(ldexp((double)a[(o + lr) * cols + c], -e));
-                col_scale[sb[g] + ((c / 128) * T + b / 4) * 512 + atom_byte(c % 128, b % 4)] = (uint8_t)(e + 127);
-            }
-        }
-    }
+    mx_quantize_f32(a, cols, off, tp, sb, G, row_data, row_scale, col_data, col_scale);
     free(a);
     free(off);
     return OR_OK;
@@ -1120,5 +1131,104 @@ int or_gemm_nvfp4_sample(int kind, const uint8_t* a_data, const uint8_t* a_scale
     }
     free(sa.buf);
     free(sb.buf);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* ScaledSwiGLU + MXFP8 quantisation of an fp32 activation                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * TransformerEngine issue 3484 names ScaledSwiGLU (with ScaledClampedQGeGLU
+ * and ScaledSiTUGLU) beside ScaledSReLU without defining it.  Reading taken:
+ * the SwiGLU of Shazeer's "GLU Variants Improve Transformer", scaled by the
+ * row's prob: the fc1 output of width 2n is split into a gate half
+ * y[:, 0:n] and a linear half y[:, n:2n], and
+ *     a[r, c] = (silu(y[r, c]) * y[r, n + c]) * probs[r],
+ *     silu(x) = x / (1 + exp(-x)),
+ * in fp32 op by op.  exp is this library's own: the argument is clamped to
+ * [-87, 88] (outside it 1 + exp(-x) is 1, or the quotient is below 1e-36),
+ * reduced by ln 2 in the Cody-Waite way (n = rint(x log2 e), r = x - n ln2_hi
+ * - n ln2_lo with fused multiply-adds, ln2_hi holding 16 bits so n ln2_hi is
+ * exact), the degree-7 Taylor polynomial of exp(r) is evaluated in Horner
+ * form with fused multiply-adds, and the result is scaled by 2^n exactly.
+ * Every step is one correctly rounded fp32 operation, so any two faithful
+ * implementations give the same bits.
+ */
+float or_act_exp(float x)
+{
+    volatile float t, n, r, p;
+    int32_t ni;
+    uint32_t bits;
+    float two_n;
+    if (x < -87.0f)
+        x = -87.0f;
+    if (x > 88.0f)
+        x = 88.0f;
+    t = x * 0x1.715476p+0f;                    /* x * log2(e), rounded */
+    n = rintf(t);
+    r = fmaf(n, -0x1.62e4p-1f, x);             /* - n * ln2_hi */
+    r = fmaf(n, -0x1.7f7d1cp-20f, r);          /* - n * ln2_lo */
+    p = 0x1.a01a02p-13f;                       /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);           /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);            /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);            /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);            /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    ni = (int32_t)n;
+    bits = (uint32_t)(ni + 127) << 23;         /* 2^n, n in [-126, 127] */
+    memcpy(&two_n, &bits, sizeof two_n);
+    return p * two_n;
+}
+
+/* silu(x) = x / (1 + exp(-x)), fp32 op by op. */
+float or_act_silu(float x)
+{
+    volatile float d = 1.0f + or_act_exp(-x);
+    return x / d;
+}
+
+/* y: fp32 [rows_cap, 2 * cols] (gate half, then linear half); the activation
+ * [rows_cap, cols] is MX-quantised rowwise and columnwise like
+ * or_quantize_mx.  Rows past the live total are neither read nor written. */
+int or_swiglu_quantize_mx(const float* y, const float* probs, int64_t rows_cap, int64_t cols,
+                          const int32_t* splits, int G, uint8_t* row_data, uint8_t* row_scale,
+                          int64_t row_scale_bytes, uint8_t* col_data, uint8_t* col_scale,
+                          int64_t col_scale_bytes)
+{
+    int64_t *off = malloc(sizeof(int64_t) * (G + 1) * 3);
+    int64_t *tp, *sb, L;
+    float* a;
+    int st;
+    if (!off)
+        return OR_ERR_INVALID_ARG;
+    tp = off + (G + 1);
+    sb = off + 2 * (G + 1);
+    st = or_split_scan(splits, G, rows_cap, cols, OR_RECIPE_MX, off, tp, sb);
+    if (st != OR_OK) {
+        free(off);
+        return st;
+    }
+    if (sb[G] > row_scale_bytes || sb[G] > col_scale_bytes) {
+        free(off);
+        return OR_ERR_INVALID_ARG;
+    }
+    L = off[G];
+    a = malloc(sizeof(float) * (size_t)(L > 0 ? L * cols : 1));
+    if (!a) {
+        free(off);
+        return OR_ERR_INVALID_ARG;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < L; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            volatile float s = or_act_silu(y[r * 2 * cols + c]);
+            volatile float t = s * y[r * 2 * cols + cols + c];
+            a[r * cols + c] = t * probs[r];
+        }
+    mx_quantize_f32(a, cols, off, tp, sb, G, row_data, row_scale, col_data, col_scale);
+    free(a);
+    free(off);
     return OR_OK;
 }
