@@ -288,6 +288,34 @@ gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w
                                     gq_stream_t stream);
 
 /*
+ * gq_gemm_fprop_swiglu_quant -- gq_gemm_fprop_srelu_quant with ScaledSwiGLU,
+ * another activation TransformerEngine issue 3484 names without defining
+ * (ScaledSwiGLU, beside ScaledClampedQGeGLU and ScaledSiTUGLU in its
+ * 'Additional context').  Reading: the SwiGLU of "GLU Variants Improve
+ * Transformer" scaled by the row's prob.  The fc1 output Y (width n) is split
+ * into a gate half Y[:, 0:n/2] and a linear half Y[:, n/2:n] (W_g's rows in
+ * the same order), and
+ *   A[r, c] = (silu(Y[r, c]) * Y[r, n/2 + c]) * probs[r],
+ *   silu(x) = x / (1 + exp(-x)),
+ * fp32 op by op, with this library's own exp: argument clamped to [-87, 88],
+ * Cody-Waite reduction by ln 2 (n = rint(x * log2(e)); r = x - n * ln2_hi -
+ * n * ln2_lo, ln2_hi = 0x1.62e4p-1, ln2_lo = 0x1.7f7d1cp-20), the degree-7
+ * Taylor polynomial of exp(r) in Horner form with fused multiply-adds, an
+ * exact scaling by 2^n.  A is MX-quantised rowwise and columnwise into
+ * act_out exactly as gq_quantize would quantise it.
+ *   y       : [R, n] of out_dtype, the pre-activation result (both halves).
+ *   act_out : MX rowwise + colwise, num_groups, rows_cap = x's rows_cap,
+ *             cols = n / 2.
+ * n must be a multiple of 256 (GQ_ERR_UNSUPPORTED otherwise); everything
+ * else as gq_gemm_fprop_srelu_quant.
+ */
+gq_status gq_gemm_fprop_swiglu_quant(const gq_quantized* x, const gq_quantized* w,
+                                     const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                                     const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
+                                     int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                                     gq_stream_t stream);
+
+/*
  * gq_gemm_dgrad -- dX_g = dY_g W_g (TransformerEngine issue 3484: M is a
  * free dimension of the dgrad).
  *   dy : MX rowwise, rows_cap R, cols n.

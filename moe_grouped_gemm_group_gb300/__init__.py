@@ -18,6 +18,7 @@ __all__ = [
     "gq_status_string", "gq_version", "gq_scale_bytes_bound", "gq_split_scan", "gq_quantize",
     "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_gemm_wgrad_noalloc", "alloc_quantized",
     "gq_gemm_fprop_bias", "gq_quantize_dbias", "gq_dbias_workspace_bytes", "gq_gemm_fprop_srelu_quant",
+    "gq_gemm_fprop_swiglu_quant",
     "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "RECIPE_NVFP4_1X16", "DTYPE_F32", "DTYPE_BF16", "STATUS",
 ]
 
@@ -96,6 +97,8 @@ def load():
                                           vp, vp]
         lib.gq_gemm_fprop_srelu_quant.restype = i32
         lib.gq_gemm_fprop_srelu_quant.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp, i32, qp, vp, vp]
+        lib.gq_gemm_fprop_swiglu_quant.restype = i32
+        lib.gq_gemm_fprop_swiglu_quant.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp, i32, qp, vp, vp]
         lib.gq_gemm_wgrad_noalloc.restype = i32
         lib.gq_gemm_wgrad_noalloc.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
         _lib = lib
@@ -281,6 +284,25 @@ def gq_gemm_fprop_srelu_quant(x: GroupedTensor, w: GroupedTensor, splits, num_gr
                                           _ptr(probs, "probs"), _ptr(y, "y"), out_dtype, C.byref(act_out.desc),
                                           _ptr(status, "status"), _stream(stream))
     _check(st, "gq_gemm_fprop_srelu_quant")
+
+
+def gq_gemm_fprop_swiglu_quant(x: GroupedTensor, w: GroupedTensor, splits, num_groups: int, n: int, k: int,
+                               probs, y, out_dtype: int, act_out: GroupedTensor, status, bias=None,
+                               stream=None) -> None:
+    """fc1 forward with ScaledSwiGLU ((silu(gate) * linear) * probs[r], gate =
+    y[:, :n/2], linear = y[:, n/2:]) and the MXFP8 row + column quantisation
+    of the [R, n/2] activation fused into the epilogue."""
+    import torch
+    bias_dtype = 0
+    if bias is not None:
+        if bias.dtype not in (torch.bfloat16, torch.float32):
+            raise ValueError(f"bias must be fp32 or bf16, got {bias.dtype}")
+        bias_dtype = DTYPE_BF16 if bias.dtype == torch.bfloat16 else DTYPE_F32
+    st = load().gq_gemm_fprop_swiglu_quant(C.byref(x.desc), C.byref(w.desc), _ptr(splits, "splits", False),
+                                           num_groups, n, k, _ptr(bias, "bias", False), bias_dtype,
+                                           _ptr(probs, "probs"), _ptr(y, "y"), out_dtype, C.byref(act_out.desc),
+                                           _ptr(status, "status"), _stream(stream))
+    _check(st, "gq_gemm_fprop_swiglu_quant")
 
 
 def gq_dbias_workspace_bytes(num_groups: int, rows_cap: int, cols: int) -> int:

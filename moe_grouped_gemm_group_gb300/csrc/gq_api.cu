@@ -390,11 +390,16 @@ gq_status gq_gemm_fprop_bias(const gq_quantized* x, const gq_quantized* w,
                       stream);
 }
 
-gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w,
-                                    const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
-                                    const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
-                                    int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
-                                    gq_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+// The fprop with a fused activation + MX quantisation of it (mode 1:
+// ScaledSReLU, activation width n; mode 2: ScaledSwiGLU, width n / 2).
+gq_status fprop_act_impl(const gq_quantized* x, const gq_quantized* w, const int32_t* d_split_sizes,
+                         int32_t num_groups, int64_t n, int64_t k, const void* d_bias, int32_t bias_dtype,
+                         const float* d_probs, void* y, int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                         gq_stream_t stream, int mode)
 {
     if (!x || !act_out || !d_probs)
         return GQ_ERR_INVALID_ARG;
@@ -404,7 +409,8 @@ gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w
         return GQ_ERR_ALIGNMENT;
     if (n % 256 != 0)
         return GQ_ERR_UNSUPPORTED;
-    if (act_out->num_groups != num_groups || act_out->rows_cap != x->rows_cap || act_out->cols != n)
+    const int64_t act_cols = mode == 2 ? n / 2 : n;
+    if (act_out->num_groups != num_groups || act_out->rows_cap != x->rows_cap || act_out->cols != act_cols)
         return GQ_ERR_SHAPE_MISMATCH;
     if (act_out->recipe.kind != GQ_RECIPE_MXFP8_1X32 || !act_out->recipe.rowwise || !act_out->recipe.colwise)
         return GQ_ERR_UNSUPPORTED;
@@ -414,14 +420,38 @@ gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w
         if (!aligned16(act_out->row_data) || !aligned16(act_out->row_scale) || !aligned16(act_out->col_data) ||
             !aligned16(act_out->col_scale))
             return GQ_ERR_ALIGNMENT;
-        const uint64_t need = mx_scale_bound(num_groups, x->rows_cap, n);
+        const uint64_t need = mx_scale_bound(num_groups, x->rows_cap, act_cols);
         if (act_out->row_scale_bytes < need || act_out->col_scale_bytes < need)
             return GQ_ERR_INVALID_ARG;
     }
     const gq::ActOutput act{d_probs, (uint8_t*)act_out->row_data, (uint8_t*)act_out->row_scale,
-                            (uint8_t*)act_out->col_data, (uint8_t*)act_out->col_scale};
+                            (uint8_t*)act_out->col_data, (uint8_t*)act_out->col_scale, mode};
     return fprop_impl(x, w, d_split_sizes, num_groups, n, k, y, out_dtype, d_bias, bias_dtype, d_status, stream,
                       &act);
+}
+
+}  // namespace
+
+extern "C" {
+
+gq_status gq_gemm_fprop_srelu_quant(const gq_quantized* x, const gq_quantized* w,
+                                    const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                                    const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
+                                    int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                                    gq_stream_t stream)
+{
+    return fprop_act_impl(x, w, d_split_sizes, num_groups, n, k, d_bias, bias_dtype, d_probs, y, out_dtype, act_out,
+                          d_status, stream, 1);
+}
+
+gq_status gq_gemm_fprop_swiglu_quant(const gq_quantized* x, const gq_quantized* w,
+                                     const int32_t* d_split_sizes, int32_t num_groups, int64_t n, int64_t k,
+                                     const void* d_bias, int32_t bias_dtype, const float* d_probs, void* y,
+                                     int32_t out_dtype, gq_quantized* act_out, int32_t* d_status,
+                                     gq_stream_t stream)
+{
+    return fprop_act_impl(x, w, d_split_sizes, num_groups, n, k, d_bias, bias_dtype, d_probs, y, out_dtype, act_out,
+                          d_status, stream, 2);
 }
 
 gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,

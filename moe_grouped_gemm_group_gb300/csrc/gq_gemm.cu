@@ -95,6 +95,9 @@ struct GemmArgs {
     uint8_t* act_row_scale = nullptr;
     uint8_t* act_col = nullptr;
     uint8_t* act_col_scale = nullptr;
+    // ScaledSwiGLU (ACT == 2): columns of the activation, n / 2; the fc1
+    // output's gate half is [0, act_half), its linear half [act_half, n)
+    int64_t act_half = 0;
 };
 
 // Four consecutive bias values of group row `g`, column `col` (col % 4 == 0).
@@ -421,6 +424,40 @@ __device__ __forceinline__ uint32_t codes4(float x0, float x1, float x2, float x
            ((uint32_t)__nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3) << 16);
 }
 
+// Transposed butterfly maximum of a warp's 32 x 32 fp32 block (lane = row,
+// x[i] = column i) on the magnitudes' bit patterns: lane j ends with the
+// largest |value| of column j.
+__device__ __forceinline__ uint32_t warp_colmax(const uint32_t (&x)[32], int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+    uint32_t m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t send = (b4 ? x[i] : x[i + 16]) & 0x7fffffffu;
+        const uint32_t keep = (b4 ? x[i + 16] : x[i]) & 0x7fffffffu;
+        m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t send = b3 ? m[i] : m[i + 8];
+        const uint32_t keep = b3 ? m[i + 8] : m[i];
+        m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t send = b2 ? m[i] : m[i + 4];
+        const uint32_t keep = b2 ? m[i + 4] : m[i];
+        m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t send = b1 ? m[i] : m[i + 2];
+        const uint32_t keep = b1 ? m[i + 2] : m[i];
+        m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+    return max(b0 ? m[1] : m[0], __shfl_xor_sync(0xffffffffu, b0 ? m[0] : m[1], 1));
+}
+
 // The fused activation of one epilogue warp: its 32 rows (lane = row, one
 // 32-row block of the group) x 128 columns of the fp32 result in v.
 // a = probs[r] * relu(y)^2 in fp32 (t = max(y, 0); t = t * t; a = t * p),
@@ -448,7 +485,6 @@ __device__ __forceinline__ void act_quant_warp(const GemmArgs& p, const Tile& t,
     }
     const int64_t row = t.row0 + 32 * q + lane;
     const float pr = __ldg(p.act_probs + row);
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
     uint32_t rword = 0;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
@@ -476,35 +512,7 @@ __device__ __forceinline__ void act_quant_warp(const GemmArgs& p, const Tile& t,
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        // columnwise: transposed butterfly max over the 32 rows (lane j ends
-        // with column j), on the magnitudes' bit patterns
-        uint32_t m[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t send = (b4 ? v[cc][i] : v[cc][i + 16]) & 0x7fffffffu;
-            const uint32_t keep = (b4 ? v[cc][i + 16] : v[cc][i]) & 0x7fffffffu;
-            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t send = b3 ? m[i] : m[i + 8];
-            const uint32_t keep = b3 ? m[i + 8] : m[i];
-            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t send = b2 ? m[i] : m[i + 4];
-            const uint32_t keep = b2 ? m[i + 4] : m[i];
-            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const uint32_t send = b1 ? m[i] : m[i + 2];
-            const uint32_t keep = b1 ? m[i + 2] : m[i];
-            m[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-        }
-        const uint32_t colmax = max(b0 ? m[1] : m[0], __shfl_xor_sync(0xffffffffu, b0 ? m[0] : m[1], 1));
-        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(colmax));
+        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(warp_colmax(v[cc], lane)));
         catom[lane * 16 + cc * 4 + q] = (uint8_t)cbyte;
         const float csc = inv_scale_of(cbyte);
         {
@@ -523,6 +531,104 @@ __device__ __forceinline__ void act_quant_warp(const GemmArgs& p, const Tile& t,
     *reinterpret_cast<uint32_t*>(ratom + lane * 16 + q * 4) = rword;
 }
 
+// exp for the fused ScaledSwiGLU, this library's own: the argument clamped
+// to [-87, 88], reduced by ln 2 in the Cody-Waite way (n = rint(x log2 e);
+// r = x - n ln2_hi - n ln2_lo, ln2_hi holding 16 bits so that n ln2_hi is
+// exact), the degree-7 Taylor polynomial of exp(r) in Horner form with fused
+// multiply-adds, and an exact scaling by 2^n.  Every step is one correctly
+// rounded fp32 operation.
+__device__ __forceinline__ float act_exp(float x)
+{
+    x = fminf(fmaxf(x, -87.f), 88.f);
+    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+    float r = __fmaf_rn(n, -0x1.62e4p-1f, x);
+    r = __fmaf_rn(n, -0x1.7f7d1cp-20f, r);
+    float y = 0x1.a01a02p-13f;
+    y = __fmaf_rn(y, r, 0x1.6c16c2p-10f);
+    y = __fmaf_rn(y, r, 0x1.111112p-7f);
+    y = __fmaf_rn(y, r, 0x1.555556p-5f);
+    y = __fmaf_rn(y, r, 0x1.555556p-3f);
+    y = __fmaf_rn(y, r, 0.5f);
+    y = __fmaf_rn(y, r, 1.f);
+    y = __fmaf_rn(y, r, 1.f);
+    return __fmul_rn(y, __int_as_float(((int)n + 127) << 23));
+}
+
+// silu(x) = x / (1 + exp(-x)), fp32 op by op.
+__device__ __forceinline__ float act_silu(float x) { return __fdiv_rn(x, __fadd_rn(1.f, act_exp(-x))); }
+
+// The fused ScaledSwiGLU of one epilogue warp: its 32 rows (lane = row, one
+// 32-row block of the group), gate columns in v[0], v[1] and the matching
+// linear columns in v[2], v[3] -- output columns [gc + 64 h, gc + 64 h + 64)
+// of the [R, act_half] activation, gc = col0 / 2.  a = (silu(g) * l) *
+// probs[r] in fp32 op by op, then MXFP8 1x32 codes and E8M0 scales rowwise
+// (2 blocks of 32 columns: bytes 2 h, 2 h + 1 of the row's atom word) and
+// columnwise (the warp's 32 rows) into the grouped layout of the [R,
+// act_half] buffer.  A warp whose rows lie past the group's end writes the
+// zero entries of its atoms and nothing else.
+__device__ __forceinline__ void act_glu_warp(const GemmArgs& p, const Tile& t, const int32_t* s_tp, int q, int h,
+                                             int lane, bool live, uint32_t (&v)[4][32])
+{
+    const int64_t nb = p.act_half / 128;
+    const int64_t gc = t.col0 / 2;
+    const int64_t cb = gc / 128;
+    const int64_t sb = 512 * nb * (int64_t)s_tp[t.g];
+    uint8_t* ratom = p.act_row_scale + sb + (t.mt * nb + cb) * 512;
+    uint8_t* catom = p.act_col_scale + sb + (cb * t.T + t.mt) * 512;
+    uint16_t* rword_at = reinterpret_cast<uint16_t*>(ratom + lane * 16 + q * 4 + 2 * h);
+    if (!live) {
+        *rword_at = 0;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+            catom[lane * 16 + (2 * h + cc) * 4 + q] = 0;
+        return;
+    }
+    const int64_t row = t.row0 + 32 * q + lane;
+    const float pr = __ldg(p.act_probs + row);
+    uint32_t rword = 0;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int64_t col = gc + 64 * h + 32 * cc;
+        uint32_t amax_r = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float a = __fmul_rn(__fmul_rn(act_silu(__uint_as_float(v[cc][i])), __uint_as_float(v[cc + 2][i])),
+                                      pr);
+            v[cc][i] = __float_as_uint(a);
+            amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
+        }
+        const uint32_t rb = e8m0_of_f32(__uint_as_float(amax_r));
+        const float rs = inv_scale_of(rb);
+        rword |= rb << (8 * cc);
+        {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]), rs, rs, rs, rs);
+            uint4* dst = reinterpret_cast<uint4*>(p.act_row + row * p.act_half + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(warp_colmax(v[cc], lane)));
+        catom[lane * 16 + (2 * h + cc) * 4 + q] = (uint8_t)cbyte;
+        const float csc = inv_scale_of(cbyte);
+        {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]),
+                              __shfl_sync(0xffffffffu, csc, 4 * i), __shfl_sync(0xffffffffu, csc, 4 * i + 1),
+                              __shfl_sync(0xffffffffu, csc, 4 * i + 2), __shfl_sync(0xffffffffu, csc, 4 * i + 3));
+            uint4* dst = reinterpret_cast<uint4*>(p.act_col + row * p.act_half + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+    *rword_at = (uint16_t)rword;
+}
+
 // Wait for the TMA writes of the last min(stages, issued) issued stages, so
 // that none lands after the CTA has left (bounded; used on every exit path).
 __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t issued,
@@ -539,8 +645,11 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int stages, int64_t 
 // ------------------------------------------------------------------------ //
 
 // ACT (fprop, BN = 256 only): the epilogue also writes the MX-quantised
-// ScaledSReLU of the result (act_quant_warp).
-template <int KIND, int BN, bool OUT_BF16, bool ACT = false>
+// activation of the result -- 1: ScaledSReLU (act_quant_warp); 2:
+// ScaledSwiGLU (act_glu_warp), where a tile holds 128 gate columns [c, c +
+// 128) and the 128 matching linear columns [act_half + c, ...), c = col0 / 2,
+// loaded as two 128-row boxes of W_g.
+template <int KIND, int BN, bool OUT_BF16, int ACT = 0>
 __global__ void __launch_bounds__(MxShape<KIND, BN>::THREADS, 1)
 k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
           const __grid_constant__ CUtensorMap tma_o, const GemmArgs p)
@@ -691,13 +800,21 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 if (KIND == GEMM_FPROP) {
                     const int64_t kb = p.k / 128;
                     ptx::tma_load_2d(sa, &tma_a, bar, kt * BK, (int32_t)t.row0);
-                    ptx::tma_load_2d(sb, &tma_b, bar, kt * BK, (int32_t)(t.g * p.n + t.col0));
+                    // ScaledSwiGLU: the tile's gate rows and its linear rows of W_g
+                    const int64_t gc = t.col0 / 2;
+                    if (ACT == 2) {
+                        ptx::tma_load_2d(sb, &tma_b, bar, kt * BK, (int32_t)(t.g * p.n + gc));
+                        ptx::tma_load_2d(sb + 16384, &tma_b, bar, kt * BK, (int32_t)(t.g * p.n + p.act_half + gc));
+                    } else {
+                        ptx::tma_load_2d(sb, &tma_b, bar, kt * BK, (int32_t)(t.g * p.n + t.col0));
+                    }
                     ptx::bulk_load(ssfa, p.sfa + 512 * (kb * c.s_tp[t.g] + t.mt * kb + kt), 512, bar);
                     const int64_t wbase = kb * (int64_t)t.g * (p.n / 128);
 #pragma unroll
-                    for (int j = 0; j < BN / 128; ++j)
-                        ptx::bulk_load(ssfb + 512 * j,
-                                       p.sfb + 512 * (wbase + (t.col0 / 128 + j) * kb + kt), 512, bar);
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int64_t ntile = ACT == 2 ? (j == 0 ? gc : p.act_half + gc) / 128 : t.col0 / 128 + j;
+                        ptx::bulk_load(ssfb + 512 * j, p.sfb + 512 * (wbase + ntile * kb + kt), 512, bar);
+                    }
                 } else if (KIND == GEMM_DGRAD) {
                     const int64_t nb = p.n / 128;
                     ptx::tma_load_2d(sa, &tma_a, bar, kt * BK, (int32_t)t.row0);
@@ -1072,10 +1189,21 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 break;
             ptx::tc_fence_after_sync();
             uint32_t v[4][32];
-            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+            // columns of TMEM chunk cc (32 wide) in Y: 128 h + 32 cc of the
+            // tile, or for ScaledSwiGLU the warp's 64 gate columns (cc = 0, 1)
+            // and the matching 64 linear columns (cc = 2, 3)
+            const int64_t gc = t.col0 / 2;
+            auto tmem_col = [&](int cc) -> uint32_t {
+                return ACT == 2 ? (uint32_t)((cc < 2 ? 0 : 128) + 64 * h + 32 * (cc & 1)) : (uint32_t)(128 * h + 32 * cc);
+            };
+            auto y_col = [&](int cc) -> int32_t {
+                return ACT == 2 ? (int32_t)((cc < 2 ? 0 : p.act_half) + gc + 64 * h + 32 * (cc & 1))
+                                : (int32_t)(t.col0 + 128 * h + 32 * cc);
+            };
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
-                ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
+                ptx::tmem_ld_32x32(tb + tmem_col(cc), v[cc]);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 ptx::tmem_wait_ld(v[cc]);
@@ -1085,17 +1213,18 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
             if (32 * q >= t.rows) {
-                if constexpr (ACT)
+                if constexpr (ACT == 1)
                     act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, false, v);
+                if constexpr (ACT == 2)
+                    act_glu_warp(p, t, c.s_tp, q, h, lane, false, v);
                 continue;
             }
             const int32_t orow = (int32_t)(t.row0 + 32 * q);
-            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
 #pragma unroll
             for (int b = 0; b < NBOX; ++b) {
                 // bias of the box's columns, added just before they are converted
                 if (KIND == GEMM_FPROP && p.bias && (OUT_BF16 || (b & 1) == 0))
-                    add_bias32(p, t.g, ocol + 32 * (OUT_BF16 ? b : b >> 1), v[OUT_BF16 ? b : b >> 1]);
+                    add_bias32(p, t.g, y_col(OUT_BF16 ? b : b >> 1), v[OUT_BF16 ? b : b >> 1]);
                 if (lane == 0)
                     ptx::bulk_wait_read_all();           // the last box's store has read it
                 __syncwarp();
@@ -1121,12 +1250,14 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::tma_store_2d(&tma_o, box, ocol + CW * b, orow);
+                    ptx::tma_store_2d(&tma_o, box, OUT_BF16 ? y_col(b) : y_col(b >> 1) + 16 * (b & 1), orow);
                     ptx::bulk_commit_group();
                 }
             }
-            if constexpr (ACT)
+            if constexpr (ACT == 1)
                 act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, true, v);
+            if constexpr (ACT == 2)
+                act_glu_warp(p, t, c.s_tp, q, h, lane, true, v);
         }
         if (lane == 0)
             ptx::bulk_wait_all();
@@ -1687,7 +1818,7 @@ cudaError_t prepare(Kernel kernel, int smem)
     return prepare_kernel(reinterpret_cast<const void*>(kernel), smem, 0, nullptr);
 }
 
-template <int KIND, int BN, bool OUT_BF16, bool ACT = false>
+template <int KIND, int BN, bool OUT_BF16, int ACT = 0>
 gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                  const GemmArgs& args, int64_t tiles_bound, cudaStream_t stream)
 {
@@ -1759,6 +1890,7 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
         args.act_row_scale = act->row_scale;
         args.act_col = act->col_data;
         args.act_col_scale = act->col_scale;
+        args.act_half = act->mode == 2 ? n / 2 : 0;
     }
     args.splits = splits;
     args.G = G;
@@ -1804,8 +1936,9 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                                               : run_mx2<GEMM_DGRAD, false>(ma, mb, msa, msb, args, bound, stream);
         }
         if (kWideTiles && n_out % 256 == 0) {
-            // 128 x 256 tiles: B of fprop travels as one 256-row box
-            if (kind == GEMM_FPROP && !make_map_u8(&mb, b.data, b.rows, b.cols, 256))
+            // 128 x 256 tiles: B of fprop travels as one 256-row box (two
+            // 128-row boxes, gate and linear rows, for ScaledSwiGLU)
+            if (kind == GEMM_FPROP && !(act && act->mode == 2) && !make_map_u8(&mb, b.data, b.rows, b.cols, 256))
                 return GQ_ERR_CUDA;
             // the output leaves in 32-row boxes of 64 bytes per row
             const bool bf16 = out_dtype == GQ_DTYPE_BF16;
@@ -1814,9 +1947,12 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                                          bf16 ? 2 : 4, out, rows_cap, n_out, bf16 ? 32 : 16, 32))
                 return GQ_ERR_CUDA;
             const int64_t bound = ((rows_cap + 127) / 128 + G) * (n_out / 256);
+            if (kind == GEMM_FPROP && act && act->mode == 2)
+                return bf16 ? run_mx<GEMM_FPROP, 256, true, 2>(ma, mb, mo, args, bound, stream)
+                            : run_mx<GEMM_FPROP, 256, false, 2>(ma, mb, mo, args, bound, stream);
             if (kind == GEMM_FPROP && act)
-                return bf16 ? run_mx<GEMM_FPROP, 256, true, true>(ma, mb, mo, args, bound, stream)
-                            : run_mx<GEMM_FPROP, 256, false, true>(ma, mb, mo, args, bound, stream);
+                return bf16 ? run_mx<GEMM_FPROP, 256, true, 1>(ma, mb, mo, args, bound, stream)
+                            : run_mx<GEMM_FPROP, 256, false, 1>(ma, mb, mo, args, bound, stream);
             if (kind == GEMM_FPROP)
                 return bf16 ? run_mx<GEMM_FPROP, 256, true>(ma, mb, mo, args, bound, stream)
                             : run_mx<GEMM_FPROP, 256, false>(ma, mb, mo, args, bound, stream);

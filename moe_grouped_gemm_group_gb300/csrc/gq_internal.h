@@ -77,14 +77,16 @@ struct GemmOperand {
 };
 enum GemmKind { GEMM_FPROP = 0, GEMM_DGRAD = 1, GEMM_WGRAD_MX = 2, GEMM_WGRAD_CHANNEL = 3 };
 
-// Outputs of the fprop with the fused ScaledSReLU + MX quantisation: per-row
+// Outputs of the fprop with a fused activation + MX quantisation: per-row
 // probs and the MX rowwise / columnwise codes and scales of the activation.
+// mode 1: ScaledSReLU (activation width n); mode 2: ScaledSwiGLU (width n / 2).
 struct ActOutput {
     const float* probs;
     uint8_t* row_data;
     uint8_t* row_scale;
     uint8_t* col_data;
     uint8_t* col_scale;
+    int mode = 1;
 };
 
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,

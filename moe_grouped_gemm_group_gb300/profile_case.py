@@ -22,6 +22,10 @@ larger than the 129 MB L2):
   quant_dbias quant fused with the per-group bias gradient (its column sums)
   fprop_act   fc1 fprop with ScaledSReLU + MX row/col quantisation of the
               activation fused into the epilogue (bf16 pre-activation out)
+  fprop_glu   fc1 fprop of width 2 x 2048 (gate and linear halves) with
+              ScaledSwiGLU + MX row/col quantisation of the [R, 2048]
+              activation fused into the epilogue
+  fprop_2f    the plain fc1 fprop of the same width 4096 (bf16 out)
 Options: --uniform replaces the workload's splits by the uniform split of
 the same live total; --store writes the wgrad result (accumulate = 0)
 instead of adding it to the main grad; --static runs the wgrad in its static
@@ -49,7 +53,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["quant", "fprop", "dgrad", "fprop2", "dgrad2", "wgrad", "wgrad64",
                                      "wgrad_ch", "fprop_bias", "quant_dbias", "fprop_act", "nv_quant",
-                                     "nv_fprop", "nv_dgrad", "nv_wgrad"])
+                                     "nv_fprop", "nv_dgrad", "nv_wgrad", "fprop_glu", "fprop_2f"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--uniform", action="store_true")
     ap.add_argument("--store", action="store_true")
@@ -125,6 +129,19 @@ def main():
         qa = gq.alloc_quantized(R, F, E, mx, dev)
         fn = lambda: gq.gq_gemm_fprop_srelu_quant(qx, qw, sp, E, F, H, probs, y, gq.DTYPE_BF16, qa,  # noqa: E731
                                                   st)
+    elif args.case in ("fprop_glu", "fprop_2f"):
+        wt = W.device_normal_bf16((E * 2 * F, H), w.seed, 0.02, 12, dev)
+        qw = quant(wt, None)
+        del wt
+        qx = quant(W.device_activation(w, H, 0, device=dev), sp)
+        y = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+        if args.case == "fprop_glu":
+            probs = torch.rand(R, device=dev)
+            qa = gq.alloc_quantized(R, F, E, mx, dev)
+            fn = lambda: gq.gq_gemm_fprop_swiglu_quant(qx, qw, sp, E, 2 * F, H, probs, y,  # noqa: E731
+                                                       gq.DTYPE_BF16, qa, st)
+        else:
+            fn = lambda: gq.gq_gemm_fprop(qx, qw, sp, E, 2 * F, H, y, gq.DTYPE_BF16, st)  # noqa: E731
     elif args.case == "fprop_bias":
         wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 10, dev)
         qw = quant(wt, None)

@@ -92,3 +92,80 @@ def test_fused_srelu_quant_refuses_narrow_outputs():
     probs = torch.ones(128, device=DEV)
     with pytest.raises(gq.GQError, match="GQ_ERR_UNSUPPORTED"):
         gq.gq_gemm_fprop_srelu_quant(xq, wq, splits_dev(splits), 1, 384, 256, probs, y, gq.DTYPE_F32, act, st)
+
+
+# --------------------------------------------------------------------------- #
+# ScaledSwiGLU (gq_gemm_fprop_swiglu_quant)                                    #
+# --------------------------------------------------------------------------- #
+
+def _run_glu(x, w, splits, G, N, K, probs, out_dtype, bias=None):
+    st = status_dev()
+    xq, _ = quantize(x, splits, G, mx_recipe(True, False), status=st)
+    wq, _ = quantize(w, None, G, mx_recipe(True, False), status=st)
+    R = x.shape[0]
+    act = gq.alloc_quantized(R, N // 2, G, mx_recipe(True, True), DEV, fill=0xAB)
+    tdt = torch.float32 if out_dtype == gq.DTYPE_F32 else torch.bfloat16
+    y = torch.full((R, N), float("nan"), dtype=tdt, device=DEV)
+    gq.gq_gemm_fprop_swiglu_quant(xq, wq, splits_dev(splits), G, N, K, probs, y, out_dtype, act, st, bias=bias)
+    check_status(st)
+    return y, act
+
+
+@pytest.mark.parametrize("splits,N,with_bias", [([96, 0, 160, 32, 256], 256, False),
+                                                 ([128, 384, 0, 32], 512, True),
+                                                 ([512], 768, True)])
+def test_fused_swiglu_quant_matches_oracle(splits, N, with_bias):
+    """Y (both halves) at the GEMMs' tolerance; the [R, N/2] activation's codes
+    and scales bit for bit against the oracle's ScaledSwiGLU + MX quantisation
+    of the GPU's own fp32 Y (the oracle computes the same exp, fp32 op by op)."""
+    splits = np.array(splits, np.int32)
+    G, L, K, pad = len(splits), int(splits.sum()), 384, 64
+    R = L + pad
+    x = np.concatenate([W.normal_bf16((L, K), 181), W.uniform_bf16((pad, K), 182, -4, 4)])
+    w = W.normal_bf16((G * N, K), 183, scale=0.08)
+    rng = np.random.default_rng(184)
+    probs_h = rng.uniform(0.0, 1.0, R).astype(np.float32)
+    probs = torch.from_numpy(probs_h).to(DEV)
+    b_bits = W.normal_bf16((G, N), 185, scale=0.5)
+    bias = bf16_dev(b_bits) if with_bias else None
+
+    y, act = _run_glu(x, w, splits, G, N, K, probs, gq.DTYPE_F32, bias)
+    yh = host(y)
+    want = O.gemm_fprop(O.quantize_mx(x, splits, G, colwise=False), O.quantize_mx(w, None, G, colwise=False),
+                        splits, G, N, K)
+    if with_bias:
+        want = O.grouped_bias_add(want, W.bf16_bits_to_f32(b_bits).astype(np.float64), splits, G)
+    off = np.concatenate([[0], np.cumsum(splits)])
+    for g in range(G):
+        a, b = int(off[g]), int(off[g + 1])
+        if b > a:
+            e = np.linalg.norm(yh[a:b] - want[a:b]) / np.linalg.norm(want[a:b])
+            assert e <= REL_TOL, f"Y group {g}: rel err {e}"
+    assert np.all(np.isnan(yh[L:]))
+
+    ref = O.swiglu_quantize_mx(np.where(np.isnan(yh), 0, yh).astype(np.float32), probs_h, splits, G)
+    assert np.array_equal(host(act.row_data)[:L], ref.row_data[:L]), "rowwise codes"
+    assert np.array_equal(host(act.col_data)[:L], ref.col_data[:L]), "columnwise codes"
+    n_scale = len(ref.row_scale)
+    assert np.array_equal(host(act.row_scale)[:n_scale], ref.row_scale), "rowwise scales"
+    assert np.array_equal(host(act.col_scale)[:n_scale], ref.col_scale), "columnwise scales"
+    assert np.all(host(act.row_data)[L:] == 0xAB) and np.all(host(act.col_data)[L:] == 0xAB)
+
+    yb, act_b = _run_glu(x, w, splits, G, N, K, probs, gq.DTYPE_BF16, bias)
+    for name in ("row_data", "col_data", "row_scale", "col_scale"):
+        assert torch.equal(getattr(act_b, name), getattr(act, name)), name
+    assert torch.equal(yb[:L].float(), y[:L].to(torch.bfloat16).float())
+
+
+def test_fused_swiglu_shape_checks():
+    splits = np.array([128], np.int32)
+    st = status_dev()
+    x = W.normal_bf16((128, 256), 186)
+    w = W.normal_bf16((512, 256), 187)
+    xq, _ = quantize(x, splits, 1, mx_recipe(True, False), status=st)
+    wq, _ = quantize(w, None, 1, mx_recipe(True, False), status=st)
+    y = torch.empty((128, 512), device=DEV)
+    probs = torch.ones(128, device=DEV)
+    wrong = gq.alloc_quantized(128, 512, 1, mx_recipe(True, True), DEV)      # must be n / 2 = 256 wide
+    with pytest.raises(gq.GQError, match="GQ_ERR_SHAPE_MISMATCH"):
+        gq.gq_gemm_fprop_swiglu_quant(xq, wq, splits_dev(splits), 1, 512, 256, probs, y, gq.DTYPE_F32, wrong, st)
