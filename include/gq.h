@@ -4,15 +4,18 @@
  *
  * The hot path has two parts:
  *   1. gq_quantize: a bf16 token buffer partitioned by split_sizes is cast to
- *      FP8 e4m3 with per-block scales, rowwise and/or columnwise.  Two
- *      recipes: MXFP8 1x32 with E8M0 scales in the swizzled
+ *      FP8 e4m3 with per-block scales, rowwise and/or columnwise.  Recipes:
+ *      MXFP8 1x32 with E8M0 scales in the swizzled
  *      [outer/128][inner/128][32][4][4] layout (TransformerEngine issue 3484,
  *      "Describe the bug"; TransformerEngine PR 3224, the group_quantize_mxfp8
- *      fix), and a per-channel 128-row fp32-scale recipe (DeepGEMM issue 365,
- *      _per_channel_cast_to_fp8).
+ *      fix), a per-channel 128-row fp32-scale recipe (DeepGEMM issue 365,
+ *      _per_channel_cast_to_fp8), and NVFP4 (E2M1 codes, 16-element E4M3
+ *      scales and a per-group fp32 scale; see GQ_RECIPE_NVFP4_1X16).
  *   2. gq_gemm_fprop / gq_gemm_dgrad / gq_gemm_wgrad: grouped GEMMs that
  *      consume those operands; the wgrad contracts only over each group's
  *      live rows (TransformerEngine issue 3484, "Additional context: Scope").
+ *      Fused variants: gq_gemm_fprop_bias, gq_quantize_dbias,
+ *      gq_gemm_fprop_srelu_quant and gq_gemm_fprop_swiglu_quant.
  *
  * Conventions shared by every call
  *  - Pointers named d_* and every buffer inside gq_quantized are DEVICE
