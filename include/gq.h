@@ -16,6 +16,8 @@
  *      live rows (TransformerEngine issue 3484, "Additional context: Scope").
  *      Fused variants: gq_gemm_fprop_bias, gq_quantize_dbias,
  *      gq_gemm_fprop_srelu_quant and gq_gemm_fprop_swiglu_quant.
+ * gq_check_wait_limit is a diagnostic: it runs the kernels' bounded-wait
+ * failure path (GQ_ERR_TIMEOUT) without a fault.
  *
  * Conventions shared by every call
  *  - Pointers named d_* and every buffer inside gq_quantized are DEVICE
@@ -395,6 +397,31 @@ gq_status gq_gemm_wgrad_noalloc(const gq_quantized* dy, const gq_quantized* x,
                                 const int32_t* d_split_sizes, int32_t num_groups, int64_t n,
                                 int64_t k, float* dw, int32_t accumulate, int32_t* d_status,
                                 gq_stream_t stream);
+
+/*
+ * gq_check_wait_limit -- a diagnostic of the library's failure path; the
+ * pages describe no such call.  Every pipeline wait in the library's kernels
+ * (an mbarrier phase: a TMA copy landing, a stage being freed, an
+ * accumulator being handed over) gives up after 2 s of device time, records
+ * GQ_ERR_TIMEOUT in *d_status (first error wins) and winds its CTA down:
+ * the other roles see a shared abort flag, in-flight copies are waited for
+ * (again bounded), tensor memory is freed, and the kernel returns.  This
+ * call runs that path on purpose, without a fault: one CTA of two warps
+ * waits on an mbarrier that nothing arrives on, until the limit passes.
+ *
+ *   d_status : device int32, 4-byte aligned, required.  Holds GQ_ERR_TIMEOUT
+ *              afterwards when it held 0 before; when it was already nonzero
+ *              the kernel does nothing (the noop flag).
+ *   d_report : NULL, or device uint64[4], 8-byte aligned: for warp w = 0, 1,
+ *              d_report[2w] = nanoseconds it waited (%globaltimer) and
+ *              d_report[2w + 1] = 1 if the barrier's phase completed, else 0
+ *              (it never completes).  Untouched by the noop path.
+ * Asynchronous on `stream`; the kernel runs for about the wait limit (2 s)
+ * and leaves the CUDA context usable.  Returns GQ_ERR_INVALID_ARG for a NULL
+ * d_status, GQ_ERR_ALIGNMENT for a misaligned pointer, GQ_ERR_CUDA when the
+ * launch fails.
+ */
+gq_status gq_check_wait_limit(int32_t* d_status, uint64_t* d_report, gq_stream_t stream);
 
 #ifdef __cplusplus
 }

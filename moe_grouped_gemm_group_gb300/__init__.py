@@ -18,7 +18,7 @@ __all__ = [
     "gq_status_string", "gq_version", "gq_scale_bytes_bound", "gq_split_scan", "gq_quantize",
     "gq_gemm_fprop", "gq_gemm_dgrad", "gq_gemm_wgrad", "gq_gemm_wgrad_noalloc", "alloc_quantized",
     "gq_gemm_fprop_bias", "gq_quantize_dbias", "gq_dbias_workspace_bytes", "gq_gemm_fprop_srelu_quant",
-    "gq_gemm_fprop_swiglu_quant",
+    "gq_gemm_fprop_swiglu_quant", "gq_check_wait_limit",
     "RECIPE_MXFP8_1X32", "RECIPE_CHANNEL128_F32", "RECIPE_NVFP4_1X16", "DTYPE_F32", "DTYPE_BF16", "STATUS",
 ]
 
@@ -101,6 +101,8 @@ def load():
         lib.gq_gemm_fprop_swiglu_quant.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp, i32, qp, vp, vp]
         lib.gq_gemm_wgrad_noalloc.restype = i32
         lib.gq_gemm_wgrad_noalloc.argtypes = [qp, qp, vp, i32, i64, i64, vp, i32, vp, vp]
+        lib.gq_check_wait_limit.restype = i32
+        lib.gq_check_wait_limit.argtypes = [vp, vp, vp]
         _lib = lib
         return lib
 
@@ -360,3 +362,13 @@ def gq_gemm_wgrad_noalloc(dy: GroupedTensor, x: GroupedTensor, splits, num_group
                                       num_groups, n, k, _ptr(dw, "dw"), int(bool(accumulate)),
                                       _ptr(status, "status"), _stream(stream))
     _check(st, "gq_gemm_wgrad_noalloc")
+
+
+def gq_check_wait_limit(status, report=None, stream=None) -> None:
+    """Run the library's bounded-wait failure path once: a wait that never
+    completes gives up after the limit and leaves GQ_ERR_TIMEOUT in
+    ``status`` (int32 CUDA tensor); ``report`` is None or a CUDA int64
+    tensor of 4 elements (per warp: nanoseconds waited, 1 if the wait
+    completed)."""
+    st = load().gq_check_wait_limit(_ptr(status, "status"), _ptr(report, "report", False), _stream(stream))
+    _check(st, "gq_check_wait_limit")

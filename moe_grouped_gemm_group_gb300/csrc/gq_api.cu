@@ -170,7 +170,7 @@ const char* gq_status_string(int32_t status)
     }
 }
 
-int32_t gq_version(void) { return (1 << 16) | 1; }
+int32_t gq_version(void) { return (1 << 16) | 2; }
 
 uint64_t gq_scale_bytes_bound(const gq_recipe* recipe, int32_t num_groups, int64_t rows_cap,
                               int64_t cols)

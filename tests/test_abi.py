@@ -211,3 +211,11 @@ def test_nvfp4_scale_bound_and_host_checks(lib):
     assert lib.gq_gemm_fprop(C.byref(x256), C.byref(mx), None, 2, 128, 256, y, 0, st, None) in (-4, -7)
     # bias with NVFP4 operands is not provided
     assert lib.gq_gemm_fprop_bias(C.byref(x), C.byref(w), None, 2, 256, 256, y, 0, y, 0, st, None) == -4
+
+
+def test_check_wait_limit_host_checks(lib):
+    """A NULL status word and misaligned pointers are refused before launch."""
+    st = C.c_void_p(0x20000)
+    assert lib.gq_check_wait_limit(None, None, None) == -1
+    assert lib.gq_check_wait_limit(C.c_void_p(0x20002), None, None) == -2
+    assert lib.gq_check_wait_limit(st, C.c_void_p(0x10004), None) == -2
