@@ -35,7 +35,8 @@
  *    the uniform split m_g = rows_cap / num_groups (rows_cap must divide;
  *    this is the single-grouped-weight case of TransformerEngine PR 3224).
  *    MX needs every m_g % 32 == 0, the per-channel recipe m_g % 128 == 0;
- *    all column counts must be multiples of 128.  1 <= num_groups <= 1024.
+ *    all column counts must be multiples of 128.  1 <= num_groups <= 1024;
+ *    0 <= rows_cap < 2^31 (a buffer may hold more than 2^31 elements).
  *  - Errors found on the host are returned synchronously and launch nothing.
  *    Errors found on the device (split sizes: negative, misaligned, or
  *    summing past rows_cap; a pipeline wait that timed out) are written to

@@ -35,7 +35,8 @@ uint64_t channel_scale_bound(int64_t rows_cap, int64_t cols)
 // Checks shared by every call on a token buffer of rows_cap rows.
 gq_status check_partition(const int32_t* d_split_sizes, int32_t G, int64_t rows_cap, int64_t cols)
 {
-    if (G < 1 || G > GQ_MAX_GROUPS || rows_cap < 0 || cols <= 0)
+    // Rows are TMA tensor-map coordinates (32-bit) in every kernel.
+    if (G < 1 || G > GQ_MAX_GROUPS || rows_cap < 0 || rows_cap >= (int64_t(1) << 31) || cols <= 0)
         return GQ_ERR_INVALID_ARG;
     if (cols % 128 != 0)
         return GQ_ERR_ALIGNMENT;

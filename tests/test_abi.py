@@ -78,6 +78,8 @@ def test_quantize_host_checks_need_no_gpu(lib):
     assert lib.gq_quantize(fake, 255, 256, None, 2, C.byref(mx), C.byref(d), st, None) == -2    # R % G
     assert lib.gq_quantize(fake, 256, 256, None, 0, C.byref(mx), C.byref(d), st, None) == -1    # G = 0
     assert lib.gq_quantize(fake, 256, 256, None, 2000, C.byref(mx), C.byref(d), st, None) == -1  # G > 1024
+    big = _desc(1, 1 << 31, 256)
+    assert lib.gq_quantize(fake, 1 << 31, 256, None, 1, C.byref(mx), C.byref(big), st, None) == -1  # rows >= 2^31
     assert lib.gq_quantize(fake, 256, 256, None, 4, C.byref(mx), C.byref(d), st, None) == -7    # descriptor G
     d2 = _desc(2, 256, 256)                                                                     # no buffers
     assert lib.gq_quantize(fake, 256, 256, None, 2, C.byref(mx), C.byref(d2), st, None) == -1

@@ -7,6 +7,11 @@ buffer compared byte for byte with the oracle, and fprop / dgrad / wgrad
 (accumulate into a fp32 main grad) compared on sampled outputs that the
 oracle computes one dot product at a time.  The sampled per-group relative
 Frobenius error must stay within 1e-5.
+
+A buffer of more than 2^31 elements ([300544, 7168] bf16) runs the same
+calls; its first and last groups are compared with the oracle run on each
+group alone (a grouped quantisation equals the single-group quantisation of
+each group's rows, bitwise: a pinned property of the oracle).
 """
 import numpy as np
 import pytest
@@ -116,3 +121,67 @@ def test_moe_e64_zipf_layer(fc):
 @pytest.mark.parametrize("fc", [1, 2])
 def test_moe_e8_layer(fc):
     run_layer("moe_e8", fc)
+
+
+def test_buffer_past_2_31_elements():
+    """X [300544, 7168] bf16 (4.3 GB; R * K > 2^31, the last group's rows
+    straddle element 2^31), dY [R, 256], three experts of width 256.  Both
+    orientations of X and dY, fprop, dgrad (dX [R, 7168] fp32, 8.6 GB) and
+    the k-grouped wgrad.  Groups 0 and 2 (1024 rows each) match the oracle on
+    that group alone: codes and scale regions byte for byte, GEMMs within
+    1e-5; the middle group's outputs are finite; the padding rows at the far
+    end of the code buffers are never written."""
+    K, N, G, R, pad = 7168, 256, 3, 300544, 128
+    L = R - pad
+    splits = np.array([1024, L - 2048, 1024], np.int32)
+    assert R * K > 2 ** 31 and (L - 1024) * K < 2 ** 31 < L * K
+    x = W.device_normal_bf16((R, K), 5, 1.0, 40, DEV)
+    dy = W.device_normal_bf16((R, N), 5, 1.0, 41, DEV)
+    wt = W.device_normal_bf16((G * N, K), 5, 0.02, 42, DEV)
+    sp = torch.as_tensor(splits).to(DEV)
+    st = status_dev()
+    mx = mx_recipe()
+    q = {k: gq.alloc_quantized(t.shape[0], t.shape[1], G, mx, DEV, fill=0xAB)
+         for k, t in (("x", x), ("dy", dy), ("w", wt))}
+    gq.gq_quantize(x, sp, G, mx, q["x"], st)
+    gq.gq_quantize(dy, sp, G, mx, q["dy"], st)
+    gq.gq_quantize(wt, None, G, mx, q["w"], st)
+    y = torch.empty((R, N), dtype=torch.float32, device=DEV)
+    dx = torch.empty((R, K), dtype=torch.float32, device=DEV)
+    dw = torch.empty((G, N, K), dtype=torch.float32, device=DEV)
+    gq.gq_gemm_fprop(q["x"], q["w"], sp, G, N, K, y, gq.DTYPE_F32, st)
+    gq.gq_gemm_dgrad(q["dy"], q["w"], sp, G, N, K, dx, gq.DTYPE_F32, st)
+    gq.gq_gemm_wgrad(q["dy"], q["x"], sp, G, N, K, dw, False, st)
+    torch.cuda.synchronize()
+    check_status(st)
+
+    def rel(got, want):
+        return np.linalg.norm(got - want) / np.linalg.norm(want)
+
+    off = np.concatenate([[0], np.cumsum(splits)])
+    for g in (0, 2):
+        a, b = int(off[g]), int(off[g + 1])
+        one = np.array([b - a], np.int32)
+        xg, dyg, wg = bits_of(x[a:b]), bits_of(dy[a:b]), bits_of(wt[g * N:(g + 1) * N])
+        for key, bits, cols in (("x", xg, K), ("dy", dyg, N)):
+            ora = O.quantize_mx(bits, one, 1)
+            sb = O.split_scan(splits, G, R, cols)[2]
+            nbytes = 512 * (cols // 128) * ((b - a + 127) // 128)
+            assert np.array_equal(host(q[key].row_data[a:b]), ora.row_data), f"{key} row codes, group {g}"
+            assert np.array_equal(host(q[key].col_data[a:b]), ora.col_data), f"{key} col codes, group {g}"
+            for t, o in ((q[key].row_scale, ora.row_scale), (q[key].col_scale, ora.col_scale)):
+                assert np.array_equal(host(t[int(sb[g]):int(sb[g]) + nbytes]), o[:nbytes]), f"{key} scales, group {g}"
+        want = O.gemm_fprop(O.quantize_mx(xg, one, 1, colwise=False), O.quantize_mx(wg, None, 1, colwise=False),
+                            one, 1, N, K)
+        assert rel(host(y[a:b]), want) <= REL_TOL, f"fprop group {g}"
+        want = O.gemm_dgrad(O.quantize_mx(dyg, one, 1, colwise=False), O.quantize_mx(wg, None, 1, rowwise=False),
+                            one, 1, N, K)
+        assert rel(host(dx[a:b]), want) <= REL_TOL, f"dgrad group {g}"
+        want = O.gemm_wgrad(O.quantize_mx(dyg, one, 1, rowwise=False), O.quantize_mx(xg, one, 1, rowwise=False),
+                            one, 1, N, K)
+        assert rel(host(dw[g]), want[0]) <= REL_TOL, f"wgrad group {g}"
+    mid = slice(int(off[1]), int(off[2]))
+    assert bool(torch.isfinite(y[mid]).all()) and bool(torch.isfinite(dx[mid]).all())
+    assert bool(torch.isfinite(dw[1]).all())
+    for key in ("x", "dy"):
+        assert bool((q[key].row_data[L:] == 0xAB).all()) and bool((q[key].col_data[L:] == 0xAB).all())
