@@ -317,3 +317,65 @@ def test_moe_e64_zipf_layer_nvfp4(fc):
     assert np.linalg.norm(got - want) <= tol, "wgrad (sampled, accumulate)"
     for e in np.flatnonzero(w.splits == 0):
         assert torch.equal(main[e], main0[e]), f"empty expert {e} changed"
+
+
+def test_buffer_past_2_31_elements_nvfp4():
+    """X [300544, 7168] bf16 (R * K > 2^31; the last group's rows straddle
+    element 2^31) on NVFP4 operands: quantisation of both orientations,
+    fprop, dgrad (dX fp32, 8.6 GB) and the k-grouped wgrad.  Groups 0 and 2
+    match the oracle run on that group alone (its amax and S_g come from the
+    group's own rows): codes, scale regions and amax bit for bit, GEMMs
+    within 1e-5; the middle group's outputs are finite."""
+    K, N, G, R, pad = 7168, 256, 3, 300544, 128
+    L = R - pad
+    splits = np.array([1024, L - 2048, 1024], np.int32)
+    assert R * K > 2 ** 31 and (L - 1024) * K < 2 ** 31 < L * K
+    x = W.device_normal_bf16((R, K), 6, 1.0, 50, DEV)
+    dy = W.device_normal_bf16((R, N), 6, 1.0, 51, DEV)
+    wt = W.device_normal_bf16((G * N, K), 6, 0.02, 52, DEV)
+    sp = torch.as_tensor(splits).to(DEV)
+    st = status_dev()
+    rec = nv_recipe()
+    q = {k: gq.alloc_quantized(t.shape[0], t.shape[1], G, rec, DEV, fill=FILL)
+         for k, t in (("x", x), ("dy", dy), ("w", wt))}
+    gq.gq_quantize(x, sp, G, rec, q["x"], st)
+    gq.gq_quantize(dy, sp, G, rec, q["dy"], st)
+    gq.gq_quantize(wt, None, G, rec, q["w"], st)
+    y = torch.empty((R, N), dtype=torch.float32, device=DEV)
+    dx = torch.empty((R, K), dtype=torch.float32, device=DEV)
+    dw = torch.empty((G, N, K), dtype=torch.float32, device=DEV)
+    gq.gq_gemm_fprop(q["x"], q["w"], sp, G, N, K, y, gq.DTYPE_F32, st)
+    gq.gq_gemm_dgrad(q["dy"], q["w"], sp, G, N, K, dx, gq.DTYPE_F32, st)
+    gq.gq_gemm_wgrad(q["dy"], q["x"], sp, G, N, K, dw, False, st)
+    torch.cuda.synchronize()
+    check_status(st)
+
+    def rel(got, want):
+        return np.linalg.norm(got - want) / np.linalg.norm(want)
+
+    off, tp, _ = O.split_scan(splits, G, R, K)
+    for g in (0, 2):
+        a, b = int(off[g]), int(off[g + 1])
+        one = np.array([b - a], np.int32)
+        xg, dyg, wg = _bits_of(x[a:b]), _bits_of(dy[a:b]), _bits_of(wt[g * N:(g + 1) * N])
+        for key, bits, cols in (("x", xg, K), ("dy", dyg, N)):
+            ora = O.quantize_nvfp4(bits, one, 1)
+            sb, nbytes = 512 * (cols // 64) * int(tp[g]), 512 * (cols // 64) * ((b - a + 127) // 128)
+            assert np.array_equal(host(q[key].row_data[a:b]), ora.row_data), f"{key} row codes, group {g}"
+            assert np.array_equal(host(q[key].col_data[:, a // 2:b // 2]), ora.col_data), f"{key} col codes, group {g}"
+            for t, o in ((q[key].row_scale, ora.row_scale), (q[key].col_scale, ora.col_scale)):
+                assert np.array_equal(host(t[sb:sb + nbytes]), o[:nbytes]), f"{key} scales, group {g}"
+            assert host(q[key].amax)[g:g + 1].view(np.uint32) == ora.amax.view(np.uint32), f"{key} amax, group {g}"
+        ow = O.quantize_nvfp4(wg, None, 1)
+        want = O.gemm_nvfp4("fprop", O.quantize_nvfp4(xg, one, 1, colwise=False), ow, one, 1, N, K)
+        assert rel(host(y[a:b]), want) <= REL_TOL, f"fprop group {g}"
+        want = O.gemm_nvfp4("dgrad", O.quantize_nvfp4(dyg, one, 1, colwise=False), ow, one, 1, N, K)
+        assert rel(host(dx[a:b]), want) <= REL_TOL, f"dgrad group {g}"
+        want = O.gemm_nvfp4("wgrad", O.quantize_nvfp4(dyg, one, 1, rowwise=False),
+                            O.quantize_nvfp4(xg, one, 1, rowwise=False), one, 1, N, K)
+        assert rel(host(dw[g]), want[0]) <= REL_TOL, f"wgrad group {g}"
+    mid = slice(int(off[1]), int(off[2]))
+    assert bool(torch.isfinite(y[mid]).all()) and bool(torch.isfinite(dx[mid]).all())
+    assert bool(torch.isfinite(dw[1]).all())
+    for key in ("x", "dy"):
+        assert bool((q[key].row_data[L:] == FILL).all()) and bool((q[key].col_data[:, L // 2:] == FILL).all())
