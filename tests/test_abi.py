@@ -221,3 +221,15 @@ def test_check_wait_limit_host_checks(lib):
     assert lib.gq_check_wait_limit(None, None, None) == -1
     assert lib.gq_check_wait_limit(C.c_void_p(0x20002), None, None) == -2
     assert lib.gq_check_wait_limit(st, C.c_void_p(0x10004), None) == -2
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libgq.so every call raises: there is no fallback path."""
+    monkeypatch.setattr(gq, "_LIB_PATH", str(tmp_path / "libgq.so"))
+    monkeypatch.setattr(gq, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        gq.load()
+    with pytest.raises(RuntimeError):
+        gq.gq_version()
+    with pytest.raises(RuntimeError):
+        gq.gq_scale_bytes_bound(gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0), 1, 128, 128)
