@@ -89,3 +89,68 @@ def rel_err_per_group(got: np.ndarray, want: np.ndarray, bounds):
         else:
             errs.append(np.linalg.norm(g - w) / nw)
     return np.array(errs)
+
+
+# --------------------------------------------------------------------------- #
+# sampled full-size checks, held to the per-group bar                          #
+# --------------------------------------------------------------------------- #
+
+def gather(t: torch.Tensor, *idx) -> np.ndarray:
+    """t[idx...] as fp64 on the host (idx: numpy index arrays)."""
+    return host(t[tuple(torch.as_tensor(np.asarray(i)).to(t.device) for i in idx)].float()).astype(np.float64)
+
+
+def stratified_rows(rng, splits, per_group: int, extra: int):
+    """Token rows to sample: `per_group` rows drawn in every non-empty group
+    (so a 32-row expert is checked as closely as the largest) plus `extra`
+    drawn uniformly over all live rows; returns (rows, group of each row)."""
+    splits = np.asarray(splits, np.int64)
+    off = np.concatenate([[0], np.cumsum(splits)])
+    rows, grp = [], []
+    for g in np.flatnonzero(splits > 0):
+        rows.append(rng.integers(off[g], off[g + 1], per_group))
+        grp.append(np.full(per_group, g))
+    if extra:
+        r = rng.integers(0, off[-1], extra)
+        rows.append(r)
+        grp.append(np.searchsorted(off, r, side="right") - 1)
+    return np.concatenate(rows), np.concatenate(grp)
+
+
+def assert_sampled_groups_close(got, want, grp, what: str, tol: float = REL_TOL):
+    """Per group: the relative Frobenius error of the sampled outputs within
+    `tol`; a group whose sampled oracle values are all 0 must give exact 0."""
+    worst = (0.0, -1)
+    for g in np.unique(grp):
+        m = grp == g
+        nw = np.linalg.norm(want[m])
+        if nw == 0:
+            assert np.all(got[m] == 0), f"{what}: group {g} should be exactly 0"
+            continue
+        e = np.linalg.norm(got[m] - want[m]) / nw
+        worst = max(worst, (e, int(g)))
+    assert worst[0] <= tol, f"{what}: group {worst[1]} sampled relative error {worst[0]:.3e} > {tol:g}"
+    return worst[0]
+
+
+def assert_sampled_increments_close(new, old, want, grp, what: str, tol: float = REL_TOL):
+    """Accumulating wgrad, per group: the increment new - old (exact in fp64
+    from the two fp32 values) against the oracle's contraction.  The kernel
+    computes new = fl32(old + acc), so |(new - old) - acc| <= 2^-24 |new|
+    element by element; that rounding is allowed per element and what is
+    left must meet the per-group bar: sum_e max(0, |new - old - want| -
+    2^-24 |new|)^2 <= tol^2 sum_e want^2."""
+    inc = new - old
+    slack = 2.0 ** -24 * np.abs(new)
+    resid = np.maximum(np.abs(inc - want) - slack, 0.0)
+    worst = (0.0, -1)
+    for g in np.unique(grp):
+        m = grp == g
+        nw = np.linalg.norm(want[m])
+        if nw == 0:
+            assert np.all(resid[m] == 0), f"{what}: group {g} increment should be exactly 0"
+            continue
+        e = np.linalg.norm(resid[m]) / nw
+        worst = max(worst, (e, int(g)))
+    assert worst[0] <= tol, f"{what}: group {worst[1]} sampled relative error {worst[0]:.3e} > {tol:g}"
+    return worst[0]
