@@ -381,18 +381,24 @@ gq_status gq_gemm_wgrad(const gq_quantized* dy, const gq_quantized* x,
  *
  * It allocates nothing.  The workspace is a GQ_WGRAD_WORKSPACE_BYTES-byte
  * array inside the library, one per device, held by every device that loads
- * the library until the process exits.  The first call on a device looks up
- * that array's device address (cudaGetSymbolAddress, with the device current)
- * and keeps it; make that first call before any stream capture.  Each call
- * clears the array's claim counter on `stream` before its kernel.  All calls
- * on a device share the one array, so calls that may overlap on the GPU (on
- * different streams without ordering between them) race and must not be
- * issued; serialise them, or use gq_gemm_wgrad with one workspace per stream.
+ * the library until the process exits.  The first call in a CUDA context
+ * looks up that array's device address there (cudaGetSymbolAddress, with the
+ * context current; if no context is current yet, this makes the device's
+ * primary context current, as any runtime call does) and keeps it, keyed by
+ * the driver's context ID, which is never reused within a process.  So any
+ * number of devices is served, and after cudaDeviceReset (a new context) the
+ * next call looks the address up again.  Make the first call in each context
+ * before any stream capture.  Each call clears the array's claim counter on
+ * `stream` before its kernel.  All calls on a device share the one array, so
+ * calls that may overlap on the GPU (on different streams without ordering
+ * between them) race and must not be issued; serialise them, or use
+ * gq_gemm_wgrad with one workspace per stream.
  *
  * Arguments, layouts, results and errors are those of gq_gemm_wgrad.  In
  * addition, a problem of 2^31 or more output tiles (num_groups * n/128 *
- * k/256, or k/128 when k % 256 != 0) exceeds the counter and returns
- * GQ_ERR_INVALID_ARG before anything is launched.
+ * k/256, or k/128 when k % 256 != 0 -- the tiles the kernel itself runs)
+ * exceeds the counter and returns GQ_ERR_INVALID_ARG before anything is
+ * launched; GQ_ERR_CUDA when the set-up above fails.
  */
 gq_status gq_gemm_wgrad_noalloc(const gq_quantized* dy, const gq_quantized* x,
                                 const int32_t* d_split_sizes, int32_t num_groups, int64_t n,

@@ -31,20 +31,16 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code)
 //
 // OffT is int64_t, or int32_t where the caller has bounded rows_cap below
 // 2^31 (offsets never pass rows_cap: a larger sum is a split error).
-//
-// With `s_tq` non-null it also receives the prefix sums of the 256-row tile
-// counts ceil(m_g / 256) (tiles of a CTA pair); s_w32 then needs 64 entries.
 template <typename OffT>
 __device__ __forceinline__ int block_scan_splits(const int32_t* __restrict__ splits, int G,
                                                  int64_t rows_cap, int align, OffT* s_off,
-                                                 int32_t* s_tp, int64_t* s_w64, int32_t* s_w32,
-                                                 int32_t* s_tq = nullptr)
+                                                 int32_t* s_tp, int64_t* s_w64, int32_t* s_w32)
 {
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
     const int nw = nt >> 5;
     const int64_t uniform = splits ? 0 : rows_cap / G;
     int64_t carry_rows = 0;
-    int32_t carry_tiles = 0, carry_pairs = 0;
+    int32_t carry_tiles = 0;
     int bad = 0;
     for (int base = 0; base < G; base += nt) {
         const int g = base + tid;
@@ -57,65 +53,49 @@ __device__ __forceinline__ int block_scan_splits(const int32_t* __restrict__ spl
                 m = 0;
         }
         const int32_t t = (int32_t)((m + 127) >> 7);
-        const int32_t u = (int32_t)((m + 255) >> 8);
         int64_t xr = m;
-        int32_t xt = t, xu = u;
+        int32_t xt = t;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int64_t yr = __shfl_up_sync(0xffffffffu, xr, d);
             const int32_t yt = __shfl_up_sync(0xffffffffu, xt, d);
-            const int32_t yu = __shfl_up_sync(0xffffffffu, xu, d);
             if (lane >= d) {
                 xr += yr;
                 xt += yt;
-                xu += yu;
             }
         }
         if (lane == 31) {
             s_w64[warp] = xr;
             s_w32[warp] = xt;
-            if (s_tq)
-                s_w32[32 + warp] = xu;
         }
         __syncthreads();
         if (warp == 0) {
             int64_t wr = lane < nw ? s_w64[lane] : 0;
             int32_t wt = lane < nw ? s_w32[lane] : 0;
-            int32_t wu = (s_tq && lane < nw) ? s_w32[32 + lane] : 0;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
                 const int64_t yr = __shfl_up_sync(0xffffffffu, wr, d);
                 const int32_t yt = __shfl_up_sync(0xffffffffu, wt, d);
-                const int32_t yu = __shfl_up_sync(0xffffffffu, wu, d);
                 if (lane >= d) {
                     wr += yr;
                     wt += yt;
-                    wu += yu;
                 }
             }
             s_w64[lane] = wr;
             s_w32[lane] = wt;
-            if (s_tq)
-                s_w32[32 + lane] = wu;
         }
         __syncthreads();
         if (g < G) {
             s_off[g] = (OffT)(carry_rows + (warp > 0 ? s_w64[warp - 1] : 0) + xr - m);
             s_tp[g] = carry_tiles + (warp > 0 ? s_w32[warp - 1] : 0) + xt - t;
-            if (s_tq)
-                s_tq[g] = carry_pairs + (warp > 0 ? s_w32[32 + warp - 1] : 0) + xu - u;
         }
         carry_rows += s_w64[nw - 1];
         carry_tiles += s_w32[nw - 1];
-        if (s_tq)
-            carry_pairs += s_w32[32 + nw - 1];
         __syncthreads();
     }
     if (tid == 0) {
         s_off[G] = (OffT)carry_rows;
         s_tp[G] = carry_tiles;
-        if (s_tq)
-            s_tq[G] = carry_pairs;
     }
     bad = __syncthreads_or(bad || carry_rows > rows_cap);
     return bad ? GQ_ERR_SPLITS : 0;

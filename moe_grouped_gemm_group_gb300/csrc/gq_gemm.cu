@@ -49,16 +49,6 @@ constexpr int BM = 128;     // MMA M (rows of the A side)
 // L2 prefetch distance of the producers, in k-tiles (tuning knob; 0 = off):
 // the operand boxes of k-tile kt + PF are prefetched into L2 when k-tile kt
 // is loaded, so that first-touch DRAM latency hides behind the smem ring.
-// How the wide wgrad adds a tile into the main grad (tuning knob): tiles of
-// at least GQ_WG_RMW_MIN_K k-tiles load the old boxes by TMA, add in
-// registers and TMA-store the sums; shorter tiles hand their boxes to TMA
-// reduce-adds at L2 (0 = always load + add + store; a large value = always
-// reduce-add).
-#ifndef GQ_WG_RMW_MIN_K
-#define GQ_WG_RMW_MIN_K 4
-#endif
-constexpr int kWgRmwMinK = GQ_WG_RMW_MIN_K;
-
 #ifndef GQ_PF_DIST
 #define GQ_PF_DIST 0
 #endif
@@ -132,6 +122,20 @@ __device__ __forceinline__ void add_bias32(const GemmArgs& p, int g, int64_t col
 #define GQ_WG_SLOTS 2
 #endif
 constexpr int kWgSlots = GQ_WG_SLOTS;
+
+// Which of the four 32-column boxes of a warp's share of a wide wgrad tile go
+// to the main grad by TMA reduce-add when accumulating (tuning knob; 0 or
+// 0xA): the others go by load + add + store.  A CTA that only loads, adds
+// and stores moves its share at about half the copy rate with two boxes in
+// flight per warp, and so does one that only reduce-adds; mixed half and
+// half, the same CTA moves about twice as much, because the reduce-adds
+// hold no load in flight.  The split matters when part of the CTAs are busy
+// with long contractions and the rest must carry the memory traffic.
+#ifndef GQ_WG_RED_MASK
+#define GQ_WG_RED_MASK 0xA
+#endif
+constexpr uint32_t kWgRedMask = GQ_WG_RED_MASK;
+static_assert(kWgRedMask == 0 || kWgRedMask == 0xA, "reduce-add boxes: none, or boxes 1 and 3");
 
 // Share of the wgrad's CTAs (percent) that claim tiles from the largest
 // groups down in the run-time order; the others start from the smallest
@@ -930,63 +934,80 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // at once (each of 8 warps takes its lane quadrant's 32 rows x 128
         // columns) and TMEM goes back to the MMA issuer before any byte moves
         // to the main grad: the next tile's MMAs overlap this tile's memory
-        // traffic, which is what bounds the k-grouped wgrad.  Each warp then
-        // sends its rows through a ring of kWgSlots 4 KB boxes (32 rows x 32 fp32,
-        // 128-byte swizzle) that lane 0 hands to the TMA unit.
+        // traffic, which is what bounds the k-grouped wgrad.  Each warp sends
+        // its rows as four 4 KB boxes (32 rows x 32 fp32, 128-byte swizzle)
+        // through kWgSlots shared-memory slots that lane 0 hands to the TMA
+        // unit.
         //   accumulate == 0: plain TMA stores.
-        //   accumulate == 1, a tile of at least kWgRmwMinK k-tiles: the old
-        //     main-grad box comes in by TMA load (the first two are issued
-        //     before the accumulator is ready), the warp adds its registers
-        //     to it in place and TMA-stores the sum.  Each warp has two boxes
-        //     in flight, so a CTA's main-grad bandwidth is bounded by the load
-        //     latency; a long contraction hides it.
-        //   accumulate == 1, a shorter tile: the TMA unit adds the box into
-        //     the main grad at L2 (reduce-add), which needs no load in flight.
-        //   Either way every element gets one round-to-nearest fp32 add, so
-        //   repeated calls are bitwise identical.
+        //   accumulate == 1: the boxes of kWgRedMask go by TMA reduce-add
+        //     (the TMA unit adds them into the main grad at L2), the others
+        //     by load + add + store: the old main-grad box comes in by TMA
+        //     load, the warp adds its registers to it in place and TMA-stores
+        //     the sum.  Either way one round-to-nearest fp32 add per element,
+        //     so repeated calls are bitwise identical.  The loads run as one
+        //     continuous stream across tiles: once a slot's store (and the
+        //     reduce-add staged in the same slot after it) has read it, the
+        //     slot is refilled with the load-add-store box kWgSlots further
+        //     on in the warp's sequence -- in the next tile when the current
+        //     one runs out, whose coordinates the warp takes one tile ahead.
+        //     So kWgSlots loads stay in flight per warp whether the tile's
+        //     contraction was long or short.
         constexpr int WBOX = 32 * 128;
         const int q = warp & 3, h = (warp - 4) >> 2, w = warp - 4;
         constexpr int WS = kWgSlots;
+        // load-add-store boxes per tile, and the position of the j-th of them
+        constexpr int NR = kWgRedMask ? 2 : 4;
+        auto rmw_pos = [](int j) { return kWgRedMask ? 2 * j : j; };
+        static_assert(WS <= NR, "a refill reaches at most one tile ahead");
         uint8_t* ring = c.out + w * WS * WBOX;
         const uint32_t ring_addr = ptx::smem_addr(ring);
         uint64_t* lbar = c.obar + WS * w;                 // load barrier of each slot
-        // box k (counted over the whole call) uses slot k & 1; per slot, bit
-        // s of lph is the parity of its next load completion and bit s of
-        // lpend says whether a load into it is in flight (lane 0's copy)
+        // per slot, bit s of lph is the parity of its next load completion
+        // and bit s of lpend says whether a load into it is in flight (lane
+        // 0's copy); load-add-store box k (counted over the call) uses slot
+        // k % WS, a plain-store box k (accumulate == 0) likewise
         uint32_t lph = 0u, lpend = 0u;
-        int64_t tiles_done = 0, boxes = 0;
+        uint32_t tiles_done = 0, boxes = 0;      // only their parity / residue matters
         bool stop = false;
         int64_t cursor = blockIdx.x, rq = 0;
-        while (!*c.abort && !stop) {
-            int64_t tile;
-            if (!dyn) {
-                tile = cursor;
-                cursor += gridDim.x;
-                if (tile >= ntiles)
-                    break;
-            } else if ((tile = ring_get<true>(ring_full, ring_empty, s_ring, rq, c.abort, p.status)) < 0) {
-                break;
-            }
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord);
-            if (t.skip)
-                continue;
-            const int32_t orow = (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q);
-            const int32_t ocol = (int32_t)(t.col0 + 128 * h);
-            const bool rmw = p.accumulate && t.nk >= kWgRmwMinK;
-            if (rmw && lane == 0) {
-                // boxes 0 and 1 of this tile: both slots, once their last
-                // stores have read them
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                for (int b = 0; b < (WS < 4 ? WS : 4); ++b) {
-                    const int slot = (int)((boxes + b) % WS);
-                    ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
-                    ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * b, orow);
-                    lpend |= 1u << slot;
+        const bool acc = p.accumulate != 0;
+        // the warp's next tile with work (an empty group with accumulate is
+        // skipped), or -1 at the end of the sequence or when a wait gave up
+        auto next_tile = [&]() -> int64_t {
+            for (;;) {
+                int64_t tile;
+                if (!dyn) {
+                    tile = cursor;
+                    cursor += gridDim.x;
+                    if (tile >= ntiles)
+                        return -1;
+                } else if ((tile = ring_get<true>(ring_full, ring_empty, s_ring, rq, c.abort, p.status)) < 0) {
+                    return -1;
                 }
+                if (!decode_tile<KIND, BN>(p, c.s_off, c.s_tp, tile, ord).skip)
+                    return tile;
             }
+        };
+        // main-grad coordinates of box b (0..3) of tile t
+        auto box_row = [&](const Tile& t) { return (int32_t)((int64_t)t.g * p.n + t.mt * BM + 32 * q); };
+        auto box_col = [&](const Tile& t, int b) { return (int32_t)(t.col0 + 128 * h + 32 * b); };
+        auto issue_load = [&](int slot, int32_t col, int32_t row) {     // lane 0
+            ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
+            ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], col, row);
+            lpend |= 1u << slot;
+        };
+        int64_t cur = next_tile();
+        if (acc && cur >= 0 && lane == 0) {
+            const Tile t0 = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
+            for (int j = 0; j < WS; ++j)
+                issue_load(j, box_col(t0, rmw_pos(j)), box_row(t0));
+        }
+        while (cur >= 0 && !stop && !*c.abort) {
+            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
+            const int32_t orow = box_row(t), ocol = box_col(t, 0);
             uint32_t v[4][32];
             if (t.nk > 0) {
-                if (!ptx::mbar_wait_warp(&c.tfull[0], (uint32_t)(tiles_done & 1), c.abort, p.status))
+                if (!ptx::mbar_wait_warp(&c.tfull[0], tiles_done & 1u, c.abort, p.status))
                     break;
                 ptx::tc_fence_after_sync();
                 const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
@@ -1001,34 +1022,28 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                 if (lane == 0)
                     ptx::mbar_arrive(&c.tempty[0]);
                 ++tiles_done;
-            } else {                                      // empty group: dW_g = 0
+            } else {                                      // empty group, accumulate = 0: dW_g = 0
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[cc][i] = 0u;
             }
+            // one tile ahead (taken once this tile's MMAs are done, so the
+            // producer has long handed it out): the refills of the last
+            // boxes go to its first boxes
+            const int64_t nxt = next_tile();
+            int32_t nrow = 0, ncol = 0;
+            if (nxt >= 0) {
+                const Tile tn = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, nxt, ord);
+                nrow = box_row(tn);
+                ncol = box_col(tn, 0);
+            }
+            if (!acc) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b, ++boxes) {
-                const int slot = (int)(boxes % WS);
-                const uint32_t box = ring_addr + slot * WBOX;
-                if (rmw) {
-                    if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
-                        stop = true;
-                        break;
-                    }
-                    lph ^= 1u << slot;
-                    lpend &= ~(1u << slot);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 o = ptx::lds128(box + ptx::swz128(lane, j));
-                        ptx::sts128(box + ptx::swz128(lane, j),
-                                    make_uint4(__float_as_uint(__uint_as_float(o.x) + __uint_as_float(v[b][4 * j])),
-                                               __float_as_uint(__uint_as_float(o.y) + __uint_as_float(v[b][4 * j + 1])),
-                                               __float_as_uint(__uint_as_float(o.z) + __uint_as_float(v[b][4 * j + 2])),
-                                               __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * j + 3]))));
-                    }
-                } else {
+                for (int b = 0; b < 4; ++b, ++boxes) {
+                    const int slot = (int)(boxes % (uint32_t)WS);
+                    const uint32_t box = ring_addr + slot * WBOX;
                     if (lane == 0) {                      // the store WS boxes back read this slot
                         if (WS == 2)
                             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -1040,24 +1055,71 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     for (int j = 0; j < 8; ++j)
                         ptx::sts128(box + ptx::swz128(lane, j),
                                     make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                cur = nxt;
+                continue;
+            }
+#pragma unroll
+            for (int j = 0; j < NR; ++j, ++boxes) {
+                const int b = rmw_pos(j);
+                const int slot = (int)(boxes % (uint32_t)WS);
+                const uint32_t box = ring_addr + slot * WBOX;
+                if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
+                    stop = true;
+                    break;
+                }
+                lph ^= 1u << slot;
+                lpend &= ~(1u << slot);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 o = ptx::lds128(box + ptx::swz128(lane, i));
+                    ptx::sts128(box + ptx::swz128(lane, i),
+                                make_uint4(__float_as_uint(__uint_as_float(o.x) + __uint_as_float(v[b][4 * i])),
+                                           __float_as_uint(__uint_as_float(o.y) + __uint_as_float(v[b][4 * i + 1])),
+                                           __float_as_uint(__uint_as_float(o.z) + __uint_as_float(v[b][4 * i + 2])),
+                                           __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * i + 3]))));
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (p.accumulate && !rmw)
-                        ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
-                    else
-                        ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
+                    ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
                     ptx::bulk_commit_group();
-                    if (rmw && b + WS < 4) {
-                        // box b + WS into this slot once the store has read it
+                }
+                if constexpr (kWgRedMask != 0) {
+                    // box b + 1 goes by reduce-add, staged in this slot once
+                    // the store has read it
+                    if (lane == 0)
                         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                        ptx::mbar_arrive_expect_tx(&lbar[slot], WBOX);
-                        ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], ocol + 32 * (b + WS), orow);
-                        lpend |= 1u << slot;
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        ptx::sts128(box + ptx::swz128(lane, i),
+                                    make_uint4(v[b + 1][4 * i], v[b + 1][4 * i + 1], v[b + 1][4 * i + 2],
+                                               v[b + 1][4 * i + 3]));
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * (b + 1), orow);
+                        ptx::bulk_commit_group();
                     }
                 }
+                // refill the slot with the load-add-store box WS further on,
+                // once what was staged in it has been read
+                if (lane == 0 && (j + WS < NR || nxt >= 0)) {
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    if (j + WS < NR)
+                        issue_load(slot, ocol + 32 * rmw_pos(j + WS), orow);
+                    else
+                        issue_load(slot, ncol + 32 * rmw_pos(j + WS - NR), nrow);
+                }
             }
+            cur = nxt;
         }
         if (lane == 0) {
             // loads still in flight (an abort) land before the CTA leaves
@@ -1314,285 +1376,12 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
     }
 }
 
-// ------------------------------------------------------------------------ //
-// MXFP8 grouped GEMM on CTA pairs (fprop, dgrad)                            //
-// ------------------------------------------------------------------------ //
-//
-// A cluster of two CTAs computes a 256 x 256 output tile with 2-SM MMAs
-// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 32): CTA r of the pair
-// holds A rows [128 r, 128 r + 128) of the tile and B rows (output columns)
-// [128 r, 128 r + 128) in its own shared memory, the full 256-column set of
-// B scale atoms, and its 128 x 256 slice of the accumulator in its own TMEM.
-// Per k-tile each CTA moves 33 KB for 2 x 128 x 256 x 128 MACs -- half the
-// operand traffic per MAC of a 128 x 128 single-CTA tile.
-//
-// Both producers signal the leader's `full` barrier (TMA with cta_group::2);
-// the leader's single MMA thread waits on it, copies the scale atoms to both
-// TMEMs, issues the MMAs, and commits stages and finished accumulators back
-// to both CTAs (multicast commit).  Epilogue warps of both CTAs drain their
-// TMEM slice (8 warps, 128 columns each), hand the accumulator back to the
-// leader, then convert and store from registers.
-
-// Whether fprop/dgrad use CTA pairs (tuning knob).
-#ifndef GQ_PAIRS
-#define GQ_PAIRS 0
-#endif
-constexpr bool kUsePairs = GQ_PAIRS != 0;
 // Whether fprop/dgrad use single-CTA 128 x 256 tiles where the output width
 // allows (tuning knob).
 #ifndef GQ_WIDE
 #define GQ_WIDE 1
 #endif
 constexpr bool kWideTiles = GQ_WIDE != 0;
-constexpr int P_BN = 256;          // N of the pair MMA (output columns per tile)
-constexpr int P_STAGE = 16384 + 16384 + 512 + 1024;   // A half, B half, SFA atom, 2 SFB atoms
-constexpr int P_STAGES = 6;
-constexpr int P_SCAN = (GQ_MAX_GROUPS + 1) * 8 + 2 * (GQ_MAX_GROUPS + 2) * 4 + 32 * 8 + 64 * 4;
-constexpr int P_BAR = 8 * (2 * P_STAGES + 3) + 16;
-constexpr int P_SMEM = 1024 + P_STAGES * P_STAGE + P_BAR + P_SCAN;
-constexpr int P_EPI_WARPS = 8;
-constexpr int P_THREADS = 128 + 32 * P_EPI_WARPS;
-constexpr uint32_t P_TMEM_COLS = 512;
-constexpr uint32_t P_SFA_COL = P_BN;          // accumulator in columns [0, 256)
-constexpr uint32_t P_SFB_COL = P_BN + 4;
-constexpr uint32_t P_SF_SLOTS = 8;            // rotating scale-factor column groups
-constexpr uint32_t P_SF_STRIDE = 12;          // A atom (4 columns) + 2 B atoms (8 columns)
-static_assert(P_SFA_COL + P_SF_SLOTS * P_SF_STRIDE <= P_TMEM_COLS, "TMEM budget");
-static_assert(P_SMEM <= kSmemLimit, "shared memory budget");
-
-struct PairArgs {
-    GemmArgs g;
-    int64_t sfa_rows;     // rows (of 256 bytes) of the scale maps
-    int64_t sfb_rows;
-};
-
-template <int KIND, bool OUT_BF16>
-__global__ void __launch_bounds__(P_THREADS, 1)
-k_gemm_mx2(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-           const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
-           const GemmArgs p)
-{
-    constexpr bool B_MN = (KIND == GEMM_DGRAD);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    uint8_t* sA = base;
-    uint8_t* sB = sA + P_STAGES * 16384;
-    uint8_t* sSFA = sB + P_STAGES * 16384;
-    uint8_t* sSFB = sSFA + P_STAGES * 512;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + P_STAGES * 1024);
-    uint64_t* empty = full + P_STAGES;
-    uint64_t* tfull = empty + P_STAGES;
-    uint64_t* tempty = tfull + 1;
-    uint64_t* drain = tempty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int64_t* s_off = reinterpret_cast<int64_t*>(tmem_slot + 4);
-    int32_t* s_tp = reinterpret_cast<int32_t*>(s_off + GQ_MAX_GROUPS + 1);
-    int32_t* s_tq = s_tp + GQ_MAX_GROUPS + 2;
-    int64_t* s_w64 = reinterpret_cast<int64_t*>(s_tq + GQ_MAX_GROUPS + 2);
-    int32_t* s_w32 = reinterpret_cast<int32_t*>(s_w64 + 32);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_rank();
-    const bool leader = rank == 0;
-    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-
-    // The status word is read once per CTA before any cluster-wide step; both
-    // CTAs of a pair see the same value unless it changes in between, in
-    // which case both still reach every cluster barrier below.
-    const bool noop = load_status(p.status) != 0;
-    const int err = noop ? 0 : block_scan_splits(p.splits, p.G, p.rows_cap, 32, s_off, s_tp,
-                                                 s_w64, s_w32, s_tq);
-    if (!noop && err && threadIdx.x == 0 && leader)
-        set_status(p.status, err);
-    const bool work = !noop && !err;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < P_STAGES; ++s) {
-            ptx::mbar_init(&full[s], 2);
-            ptx::mbar_init(&empty[s], 1);
-        }
-        ptx::mbar_init(tfull, 1);
-        ptx::mbar_init(tempty, 2 * P_EPI_WARPS);
-        ptx::mbar_init(drain, 1);
-        *abort = 0;
-        ptx::fence_barrier_init();
-    }
-    if (warp == 1) {
-        ptx::tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
-        ptx::tmem_relinquish_pair();
-    }
-    if (warp == 0 && lane == 0) {
-        ptx::prefetch_tmap(&tma_a);
-        ptx::prefetch_tmap(&tma_b);
-        ptx::prefetch_tmap(&tma_sfa);
-        ptx::prefetch_tmap(&tma_sfb);
-    }
-    ptx::tc_fence_before_sync();
-    ptx::cluster_sync();
-    ptx::tc_fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-
-    const int64_t nnt = (KIND == GEMM_FPROP ? p.n : p.k) / P_BN;
-    const int64_t ntiles = work ? (int64_t)s_tq[p.G] * nnt : 0;
-    const int nk = (int)((KIND == GEMM_FPROP ? p.k : p.n) / BK);
-    const int64_t kb = nk;                                   // 128-deep k-tiles = scale atoms per row tile
-    const uint32_t full0 = ptx::map_to_cta(ptx::smem_addr(&full[0]), 0);
-    const uint32_t tempty0 = ptx::map_to_cta(ptx::smem_addr(tempty), 0);
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA producer --
-        int64_t issued = 0;
-        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
-            const int64_t rt = tile / nnt, nt = tile - rt * nnt;
-            const int g = group_of_tile(s_tq, p.G, rt);
-            const int64_t mt128 = 2 * (rt - s_tq[g]) + rank;        // this CTA's 128-row tile
-            const int32_t row0 = (int32_t)(s_off[g] + 128 * mt128);
-            const int64_t col0 = nt * P_BN;
-            bool ok = true;
-            for (int kt = 0; kt < nk; ++kt, ++issued) {
-                const int s = (int)(issued % P_STAGES);
-                const uint32_t ph = (uint32_t)((issued / P_STAGES) & 1);
-                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort, p.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bar = full0 + 8u * s;
-                if (PF_DIST > 0 && kt + PF_DIST < nk) {
-                    const int kp = kt + PF_DIST;
-                    ptx::tma_prefetch_l2_2d(&tma_a, kp * BK, row0);
-                    if (KIND == GEMM_FPROP)
-                        ptx::tma_prefetch_l2_2d(&tma_b, kp * BK, (int32_t)(g * p.n + col0 + 128 * rank));
-                    else
-                        ptx::tma_prefetch_l2_2d(&tma_b, (int32_t)(col0 + 128 * rank), (int32_t)(g * p.n + kp * BK));
-                }
-                ptx::mbar_arrive_expect_tx_cluster(bar, P_STAGE);
-                ptx::tma_load_2d_pair(sA + s * 16384, &tma_a, bar, kt * BK, row0);
-                // scale atoms as rows of 256 bytes: atom a = rows 2a, 2a + 1
-                if (KIND == GEMM_FPROP) {
-                    ptx::tma_load_2d_pair(sB + s * 16384, &tma_b, bar, kt * BK,
-                                          (int32_t)(g * p.n + col0 + 128 * rank));
-                    ptx::tma_load_2d_pair(sSFA + s * 512, &tma_sfa, bar, 0,
-                                          (int32_t)(2 * (kb * s_tp[g] + mt128 * kb + kt)));
-                    const int64_t wbase = kb * (int64_t)g * (p.n / 128);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        ptx::tma_load_2d_pair(sSFB + s * 1024 + 512 * j, &tma_sfb, bar, 0,
-                                              (int32_t)(2 * (wbase + (col0 / 128 + j) * kb + kt)));
-                } else {
-                    const int64_t nb = p.n / 128;
-                    ptx::tma_load_2d_pair(sB + s * 16384, &tma_b, bar, (int32_t)(col0 + 128 * rank),
-                                          (int32_t)(g * p.n + kt * BK));
-                    ptx::tma_load_2d_pair(sSFA + s * 512, &tma_sfa, bar, 0,
-                                          (int32_t)(2 * (nb * s_tp[g] + mt128 * nb + kt)));
-                    const int64_t wbase = (p.k / 128) * (int64_t)g * nb;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        ptx::tma_load_2d_pair(sSFB + s * 1024 + 512 * j, &tma_sfb, bar, 0,
-                                              (int32_t)(2 * (wbase + (col0 / 128 + j) * nb + kt)));
-                }
-            }
-            if (!ok)
-                break;
-        }
-        if (leader) {
-            volatile int no_abort = 0;
-            for (int64_t q = issued - P_STAGES < 0 ? 0 : issued - P_STAGES; q < issued; ++q)
-                if (!ptx::mbar_wait(&full[q % P_STAGES], (uint32_t)((q / P_STAGES) & 1), &no_abort, p.status))
-                    break;
-        }
-    } else if (warp == 1 && lane == 0 && leader) {
-        // ---------------------------------------- MMA issuer (leader) --
-        int64_t consumed = 0, tiles_done = 0;
-        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
-            if (!ptx::mbar_wait(tempty, (uint32_t)((tiles_done & 1) ^ 1), abort, p.status))
-                break;
-            ptx::tc_fence_after_sync();
-            bool ok = true;
-            for (int kt = 0; kt < nk; ++kt, ++consumed) {
-                const int s = (int)(consumed % P_STAGES);
-                const uint32_t ph = (uint32_t)((consumed / P_STAGES) & 1);
-                if (!ptx::mbar_wait(&full[s], ph, abort, p.status)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after_sync();
-                const uint32_t sf_off = (uint32_t)(consumed % P_SF_SLOTS) * P_SF_STRIDE;
-                ptx::tc_cp_sf_atom_pair(tmem + P_SFA_COL + sf_off,
-                                        ptx::smem_desc(ptx::smem_addr(sSFA + s * 512), 0, 128, 0));
-                ptx::tc_cp_sf_atom_pair(tmem + P_SFB_COL + sf_off,
-                                        ptx::smem_desc(ptx::smem_addr(sSFB + s * 1024), 0, 128, 0));
-                ptx::tc_cp_sf_atom_pair(tmem + P_SFB_COL + sf_off + 4,
-                                        ptx::smem_desc(ptx::smem_addr(sSFB + s * 1024 + 512), 0, 128, 0));
-                const uint32_t a_addr = ptx::smem_addr(sA + s * 16384);
-                const uint32_t b_addr = ptx::smem_addr(sB + s * 16384);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint64_t ad = ptx::smem_desc(a_addr + 32 * j, 16, 1024, 2);
-                    const uint64_t bd = B_MN ? ptx::smem_desc(b_addr + 4096 * j, 16384, 1024, 2)
-                                             : ptx::smem_desc(b_addr + 32 * j, 16, 1024, 2);
-                    ptx::tc_mma_mxf8_pair(tmem, ad, bd, ptx::idesc_mxf8(256, P_BN, 0, B_MN, (uint32_t)j),
-                                          tmem + P_SFA_COL + sf_off, tmem + P_SFB_COL + sf_off, (kt | j) != 0);
-                }
-                ptx::tc_commit_pair(&empty[s], 0x3);
-            }
-            if (!ok)
-                break;
-            ptx::tc_commit_pair(tfull, 0x3);
-            ++tiles_done;
-        }
-        ptx::tc_commit_pair(drain, 0x1);
-        volatile int no_abort = 0;
-        ptx::mbar_wait(drain, 0, &no_abort, p.status);
-    } else if (warp >= 4) {
-        // --------------------------------------------------- epilogue --
-        const int q = warp & 3, h = (warp - 4) >> 2;            // lane quadrant, column half
-        const int r = 32 * q + lane;                             // row of this CTA's slice
-        int64_t tiles_done = 0;
-        const int64_t ld = KIND == GEMM_FPROP ? p.n : p.k;
-        for (int64_t tile = pair; tile < ntiles && !*abort; tile += npairs) {
-            const int64_t rt = tile / nnt, nt = tile - rt * nnt;
-            const int g = group_of_tile(s_tq, p.G, rt);
-            const int64_t m = s_off[g + 1] - s_off[g];
-            const int64_t lr = 256 * (rt - s_tq[g]) + 128 * rank + r;   // row inside the group
-            const bool live = lr < m;
-            if (!ptx::mbar_wait(tfull, (uint32_t)(tiles_done & 1), abort, p.status))
-                break;
-            ptx::tc_fence_after_sync();
-            uint32_t v[4][32];
-            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                ptx::tmem_ld_32x32(tb + 32 * c, v[c]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                ptx::tmem_wait_ld(v[c]);
-            ptx::tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive_cluster(tempty0);
-            ++tiles_done;
-            if (live) {
-                const int64_t off = (s_off[g] + lr) * ld + nt * P_BN + 128 * h;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (OUT_BF16)
-                        store_row_bf16(static_cast<uint16_t*>(p.out) + off + 32 * c, v[c]);
-                    else
-                        store_row_f32(static_cast<float*>(p.out) + off + 32 * c, v[c]);
-                }
-            }
-        }
-    }
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    ptx::cluster_sync();
-    if (warp == 1) {
-        __syncwarp();
-        ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc_pair(tmem, P_TMEM_COLS);
-    }
-}
 
 // ------------------------------------------------------------------------ //
 // Per-channel 128-row fp32-scale k-grouped wgrad                            //
@@ -1833,47 +1622,13 @@ gq_status run_mx(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap
     return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 
-template <int KIND, bool OUT_BF16>
-gq_status run_mx2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
-                  const CUtensorMap& msb, const GemmArgs& args, int64_t pair_tiles_bound,
-                  cudaStream_t stream)
-{
-    auto kernel = k_gemm_mx2<KIND, OUT_BF16>;
-    if (prepare(kernel, P_SMEM) != cudaSuccess)
-        return GQ_ERR_CUDA;
-    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_bound, device_info().sm_count / 2));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-    cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = P_SMEM;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, ma, mb, msa, msb, args) != cudaSuccess)
-        return GQ_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
-}
-
-// Bytes of an MX scale buffer for G groups over `rows` rows (the ABI bound).
-uint64_t mx_scale_bytes(int G, int64_t rows, int64_t cols)
-{
-    return 512ull * (uint64_t)(cols / 128) * (uint64_t)((rows + 127) / 128 + G);
-}
-
-// Scale buffer of `bytes` bytes viewed as rows of 256 bytes (an atom is two
-// rows), so that scale atoms travel by TMA with the pair's barrier.
-bool make_scale_map(CUtensorMap* map, const void* base, uint64_t bytes)
-{
-    return make_tensor_map_2d_plain(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base,
-                                    (int64_t)(bytes / 256), 256, 256, 2);
-}
-
 }  // namespace
+
+int64_t wgrad_mx_tiles(int G, int64_t n, int64_t k)
+{
+    const bool wide = kWideTiles && k % 256 == 0;
+    return (int64_t)G * (n / 128) * (k / (wide ? 256 : 128));
+}
 
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
@@ -1921,20 +1676,6 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
             return GQ_ERR_CUDA;
         if (act && (kind != GEMM_FPROP || !kWideTiles || n_out % 256 != 0))
             return GQ_ERR_UNSUPPORTED;
-        if (kUsePairs && !bias && !act && n_out % P_BN == 0 && device_info().sm_count >= 2) {
-            // CTA pairs on 256 x 256 tiles; scale atoms by TMA (rows of 256 bytes)
-            CUtensorMap msa, msb;
-            const uint64_t sa = std::min<uint64_t>(a.scale_bytes, mx_scale_bytes(G, a.rows, a.cols));
-            const uint64_t sb = std::min<uint64_t>(b.scale_bytes, mx_scale_bytes(G, b.rows, b.cols));
-            if (!make_scale_map(&msa, a.scale, sa) || !make_scale_map(&msb, b.scale, sb))
-                return GQ_ERR_CUDA;
-            const int64_t bound = ((rows_cap + 255) / 256 + G) * (n_out / P_BN);
-            if (kind == GEMM_FPROP)
-                return out_dtype == GQ_DTYPE_BF16 ? run_mx2<GEMM_FPROP, true>(ma, mb, msa, msb, args, bound, stream)
-                                                  : run_mx2<GEMM_FPROP, false>(ma, mb, msa, msb, args, bound, stream);
-            return out_dtype == GQ_DTYPE_BF16 ? run_mx2<GEMM_DGRAD, true>(ma, mb, msa, msb, args, bound, stream)
-                                              : run_mx2<GEMM_DGRAD, false>(ma, mb, msa, msb, args, bound, stream);
-        }
         if (kWideTiles && n_out % 256 == 0) {
             // 128 x 256 tiles: B of fprop travels as one 256-row box (two
             // 128-row boxes, gate and linear rows, for ScaledSwiGLU)
@@ -1971,7 +1712,7 @@ gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
             return GQ_ERR_CUDA;
         CUtensorMap mo;
         const bool wide = kWideTiles && k % 256 == 0;    // 32-row boxes per warp, else 128-row boxes
-        const int64_t ntiles = (int64_t)G * (n / 128) * (k / (wide ? 256 : 128));
+        const int64_t ntiles = wgrad_mx_tiles(G, n, k);
         if (workspace && ntiles < (int64_t(1) << 31)) {
             // run-time tile order: the claim counter starts at zero
             if (cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), stream) != cudaSuccess)

@@ -89,6 +89,11 @@ struct ActOutput {
     int mode = 1;
 };
 
+// Output tiles of the k-grouped MX wgrad over G groups of an [n, k] weight:
+// G * n/128 * k/256 when the launcher takes 256-wide tiles, else
+// G * n/128 * k/128.  The tile-claim counter counts them in 32-bit halves.
+int64_t wgrad_mx_tiles(int G, int64_t n, int64_t k);
+
 gq_status launch_gemm(GemmKind kind, const GemmOperand& a, const GemmOperand& b,
                       const int32_t* splits, int G, int64_t rows_cap, int64_t n, int64_t k,
                       void* out, int out_dtype, int accumulate, int32_t* status,

@@ -5,14 +5,18 @@
 // bytes.  Every device that loads the library holds one copy of it until the
 // process exits.  Host code must not pass the array's name to a kernel (on
 // the host it names a stand-in object, not device memory): the device address
-// is looked up once per device with cudaGetSymbolAddress, with that device
-// current, and handed to the regular entry point as its workspace.
+// is looked up with cudaGetSymbolAddress once per CUDA context, on the first
+// call made with that context current, and handed to the regular entry point
+// as its workspace.
 
-#include <mutex>
-
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "gq.h"
+#include <mutex>
+#include <vector>
+
+#include "gq_internal.h"
 
 namespace {
 
@@ -20,29 +24,73 @@ namespace {
 // every call clears them on its stream before the kernel runs.
 static __device__ __align__(256) unsigned char g_wgrad_scratch[GQ_WGRAD_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
+// The address of the array is a property of the context it was looked up in:
+// a device reset or a second context on the same device loads the module
+// again, at another address.  Cached addresses are keyed by the driver's
+// context ID, which is unique for the life of the process (a handle value can
+// be reused after its context is destroyed; an ID cannot).
+struct Entry {
+    unsigned long long ctx_id;
+    void* addr;
+};
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+std::vector<Entry> g_addr;
 
-// Device address of the scratch array on the current device (looked up on
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// The current context's ID from the driver (taken at run time, like the
+// tensor-map encoder, so that loading the library needs no GPU).
+bool current_context_id(unsigned long long* id)
+{
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PfnCtxGetCurrent>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PfnCtxGetId>(p);
+    });
+    if (!get_current || !get_id)
+        return false;
+    CUcontext ctx = nullptr;
+    return get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context (looked up on
 // the first call there), or nullptr with *err set.
 void* scratch_address(gq_status* err)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);     // false while no context is current
+    if (have_id) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (const Entry& e : g_addr)
+            if (e.ctx_id == id)
+                return e.addr;
+    }
+    // set-up in this context (a runtime call: it makes the device's primary
+    // context current when none was)
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wgrad_scratch) != cudaSuccess || !p) {
+        *err = GQ_ERR_CUDA;
+        return nullptr;
+    }
+    if (!have_id && !current_context_id(&id)) {
         *err = GQ_ERR_CUDA;
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_wgrad_scratch) != cudaSuccess || !p) {
-            *err = GQ_ERR_CUDA;
-            return nullptr;
-        }
-        g_addr[dev] = p;
-    }
-    return g_addr[dev];
+    for (const Entry& e : g_addr)
+        if (e.ctx_id == id)
+            return e.addr;
+    g_addr.push_back(Entry{id, p});
+    return p;
 }
 
 }  // namespace
@@ -53,12 +101,10 @@ extern "C" gq_status gq_gemm_wgrad_noalloc(const gq_quantized* dy, const gq_quan
                                            int32_t* d_status, gq_stream_t stream)
 {
     // The claim counter counts tiles in 32-bit halves: larger problems are
-    // refused rather than run in another order.
-    if (num_groups >= 1 && n > 0 && k > 0 && n % 128 == 0 && k % 128 == 0) {
-        const int64_t tiles = (int64_t)num_groups * (n / 128) * (k / (k % 256 == 0 ? 256 : 128));
-        if (tiles >= (int64_t(1) << 31))
-            return GQ_ERR_INVALID_ARG;
-    }
+    // refused rather than run in another order (the count is the launcher's).
+    if (num_groups >= 1 && n > 0 && k > 0 && n % 128 == 0 && k % 128 == 0 &&
+        gq::wgrad_mx_tiles(num_groups, n, k) >= (int64_t(1) << 31))
+        return GQ_ERR_INVALID_ARG;
     gq_status err = GQ_OK;
     void* ws = scratch_address(&err);
     if (!ws)

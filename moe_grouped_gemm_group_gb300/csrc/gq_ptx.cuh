@@ -384,106 +384,5 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32])
                  : "memory");
 }
 
-// ----------------------------------------------- CTA pairs (cta_group::2) --
-//
-// A cluster of two CTAs runs one 2-SM MMA: the leader (rank 0) issues every
-// tcgen05 operation of the pair; shared-memory descriptors and TMEM addresses
-// refer to the same offsets in both CTAs.
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Shared::cluster address of the object at shared address `addr` in CTA `rank`.
-__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank)
-{
-    uint32_t out;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-    return out;
-}
-
-// Arrive (with expected transaction bytes) on an mbarrier given by its
-// shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cbar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
-}
-
-// 2-D tiled load into this CTA's shared memory whose completion is signalled
-// on the mbarrier at shared::cluster address `cbar` (the pair leader's).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t cbar,
-                                                 int32_t x, int32_t y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cbar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(dst)),
-                 "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair()
-{
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-// Arrive on the mbarrier at shared offset `bar` in every CTA of `mask` once
-// all prior tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_cp_sf_atom_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                                 uint32_t sfa, uint32_t sfb, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
-        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-        : "memory");
-}
-
 }  // namespace ptx
 }  // namespace gq
