@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "gq_internal.h"
 #include "gq_ptx.cuh"
@@ -123,19 +124,21 @@ __device__ __forceinline__ void add_bias32(const GemmArgs& p, int g, int64_t col
 #endif
 constexpr int kWgSlots = GQ_WG_SLOTS;
 
-// Which of the four 32-column boxes of a warp's share of a wide wgrad tile go
-// to the main grad by TMA reduce-add when accumulating (tuning knob; 0 or
-// 0xA): the others go by load + add + store.  A CTA that only loads, adds
-// and stores moves its share at about half the copy rate with two boxes in
-// flight per warp, and so does one that only reduce-adds; mixed half and
-// half, the same CTA moves about twice as much, because the reduce-adds
-// hold no load in flight.  The split matters when part of the CTAs are busy
-// with long contractions and the rest must carry the memory traffic.
-#ifndef GQ_WG_RED_MASK
-#define GQ_WG_RED_MASK 0xA
+// How the accumulating wide wgrad moves a tile into the main grad.  Each
+// warp's share is four 32-column boxes; either all four go by load + add +
+// store, or boxes 1 and 3 go by TMA reduce-add and the others by load + add
+// + store.  Measured on a 3.8 GB fp32 buffer: when every SM carries main-grad
+// traffic, load + add + store alone reaches the copy rate and the mix falls
+// short of it; when only half of the SMs do (the others busy with long
+// contractions), load + add + store alone and reduce-add alone each move
+// about 70% of the copy rate and the mix about 100%, because the reduce-adds
+// hold no load in flight.  So the kernel mixes when the split sizes are
+// skewed: when the largest group holds at least GQ_WG_MIX_SKEW times the
+// mean live group (tuning knob; 0 = always mix, a huge value = never).
+#ifndef GQ_WG_MIX_SKEW
+#define GQ_WG_MIX_SKEW 4
 #endif
-constexpr uint32_t kWgRedMask = GQ_WG_RED_MASK;
-static_assert(kWgRedMask == 0 || kWgRedMask == 0xA, "reduce-add boxes: none, or boxes 1 and 3");
+constexpr int64_t kWgMixSkew = GQ_WG_MIX_SKEW;
 
 // Share of the wgrad's CTAs (percent) that claim tiles from the largest
 // groups down in the run-time order; the others start from the smallest
@@ -939,9 +942,10 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         // through kWgSlots shared-memory slots that lane 0 hands to the TMA
         // unit.
         //   accumulate == 0: plain TMA stores.
-        //   accumulate == 1: the boxes of kWgRedMask go by TMA reduce-add
-        //     (the TMA unit adds them into the main grad at L2), the others
-        //     by load + add + store: the old main-grad box comes in by TMA
+        //   accumulate == 1: with skewed splits (kWgMixSkew) boxes 1 and 3 go
+        //     by TMA reduce-add (the TMA unit adds them into the main grad at
+        //     L2), the others by load + add + store: the old main-grad box
+        //     comes in by TMA
         //     load, the warp adds its registers to it in place and TMA-stores
         //     the sum.  Either way one round-to-nearest fp32 add per element,
         //     so repeated calls are bitwise identical.  The loads run as one
@@ -955,10 +959,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
         constexpr int WBOX = 32 * 128;
         const int q = warp & 3, h = (warp - 4) >> 2, w = warp - 4;
         constexpr int WS = kWgSlots;
-        // load-add-store boxes per tile, and the position of the j-th of them
-        constexpr int NR = kWgRedMask ? 2 : 4;
-        auto rmw_pos = [](int j) { return kWgRedMask ? 2 * j : j; };
-        static_assert(WS <= NR, "a refill reaches at most one tile ahead");
+        static_assert(WS <= 2, "a refill reaches at most one tile ahead");
         uint8_t* ring = c.out + w * WS * WBOX;
         const uint32_t ring_addr = ptx::smem_addr(ring);
         uint64_t* lbar = c.obar + WS * w;                 // load barrier of each slot
@@ -996,131 +997,152 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             ptx::tma_load_2d(ring + slot * WBOX, &tma_o, &lbar[slot], col, row);
             lpend |= 1u << slot;
         };
-        int64_t cur = next_tile();
-        if (acc && cur >= 0 && lane == 0) {
-            const Tile t0 = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
-            for (int j = 0; j < WS; ++j)
-                issue_load(j, box_col(t0, rmw_pos(j)), box_row(t0));
-        }
-        while (cur >= 0 && !stop && !*c.abort) {
-            const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
-            const int32_t orow = box_row(t), ocol = box_col(t, 0);
-            uint32_t v[4][32];
-            if (t.nk > 0) {
-                if (!ptx::mbar_wait_warp(&c.tfull[0], tiles_done & 1u, c.abort, p.status))
-                    break;
-                ptx::tc_fence_after_sync();
-                const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    ptx::tmem_wait_ld(v[cc]);
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(&c.tempty[0]);
-                ++tiles_done;
-            } else {                                      // empty group, accumulate = 0: dW_g = 0
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[cc][i] = 0u;
+        // MIX: boxes 1 and 3 of a warp's share go by reduce-add; NR
+        // load-add-store boxes a tile, the j-th of them at box rmw_pos(j)
+        auto epilogue = [&](auto mix_c) {
+            constexpr bool MIX = decltype(mix_c)::value;
+            constexpr int NR = MIX ? 2 : 4;
+            auto rmw_pos = [](int j) { return MIX ? 2 * j : j; };
+            int64_t cur = next_tile();
+            if (acc && cur >= 0 && lane == 0) {
+                const Tile t0 = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
+                for (int j = 0; j < WS; ++j)
+                    issue_load(j, box_col(t0, rmw_pos(j)), box_row(t0));
             }
-            // one tile ahead (taken once this tile's MMAs are done, so the
-            // producer has long handed it out): the refills of the last
-            // boxes go to its first boxes
-            const int64_t nxt = next_tile();
-            int32_t nrow = 0, ncol = 0;
-            if (nxt >= 0) {
-                const Tile tn = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, nxt, ord);
-                nrow = box_row(tn);
-                ncol = box_col(tn, 0);
-            }
-            if (!acc) {
-#pragma unroll
-                for (int b = 0; b < 4; ++b, ++boxes) {
+            while (cur >= 0 && !stop && !*c.abort) {
+                const Tile t = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, cur, ord);
+                const int32_t orow = box_row(t), ocol = box_col(t, 0);
+                uint32_t v[4][32];
+                if (t.nk > 0) {
+                    if (!ptx::mbar_wait_warp(&c.tfull[0], tiles_done & 1u, c.abort, p.status))
+                        break;
+                    ptx::tc_fence_after_sync();
+                    const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
+    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        ptx::tmem_wait_ld(v[cc]);
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&c.tempty[0]);
+                    ++tiles_done;
+                } else {                                      // empty group, accumulate = 0: dW_g = 0
+    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[cc][i] = 0u;
+                }
+                // one tile ahead (taken once this tile's MMAs are done, so the
+                // producer has long handed it out): the refills of the last
+                // boxes go to its first boxes
+                const int64_t nxt = next_tile();
+                int32_t nrow = 0, ncol = 0;
+                if (nxt >= 0) {
+                    const Tile tn = decode_tile<KIND, BN>(p, c.s_off, c.s_tp, nxt, ord);
+                    nrow = box_row(tn);
+                    ncol = box_col(tn, 0);
+                }
+                if (!acc) {
+    #pragma unroll
+                    for (int b = 0; b < 4; ++b, ++boxes) {
+                        const int slot = (int)(boxes % (uint32_t)WS);
+                        const uint32_t box = ring_addr + slot * WBOX;
+                        if (lane == 0) {                      // the store WS boxes back read this slot
+                            if (WS == 2)
+                                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                            else
+                                asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+                        }
+                        __syncwarp();
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ptx::sts128(box + ptx::swz128(lane, j),
+                                        make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    cur = nxt;
+                    continue;
+                }
+    #pragma unroll
+                for (int j = 0; j < NR; ++j, ++boxes) {
+                    const int b = rmw_pos(j);
                     const int slot = (int)(boxes % (uint32_t)WS);
                     const uint32_t box = ring_addr + slot * WBOX;
-                    if (lane == 0) {                      // the store WS boxes back read this slot
-                        if (WS == 2)
-                            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                        else
-                            asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+                    if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
+                        stop = true;
+                        break;
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        ptx::sts128(box + ptx::swz128(lane, j),
-                                    make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
+                    lph ^= 1u << slot;
+                    lpend &= ~(1u << slot);
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 o = ptx::lds128(box + ptx::swz128(lane, i));
+                        ptx::sts128(box + ptx::swz128(lane, i),
+                                    make_uint4(__float_as_uint(__uint_as_float(o.x) + __uint_as_float(v[b][4 * i])),
+                                               __float_as_uint(__uint_as_float(o.y) + __uint_as_float(v[b][4 * i + 1])),
+                                               __float_as_uint(__uint_as_float(o.z) + __uint_as_float(v[b][4 * i + 2])),
+                                               __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * i + 3]))));
+                    }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
                         ptx::bulk_commit_group();
                     }
-                }
-                cur = nxt;
-                continue;
-            }
-#pragma unroll
-            for (int j = 0; j < NR; ++j, ++boxes) {
-                const int b = rmw_pos(j);
-                const int slot = (int)(boxes % (uint32_t)WS);
-                const uint32_t box = ring_addr + slot * WBOX;
-                if (!ptx::mbar_wait_warp(&lbar[slot], (lph >> slot) & 1u, c.abort, p.status)) {
-                    stop = true;
-                    break;
-                }
-                lph ^= 1u << slot;
-                lpend &= ~(1u << slot);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 o = ptx::lds128(box + ptx::swz128(lane, i));
-                    ptx::sts128(box + ptx::swz128(lane, i),
-                                make_uint4(__float_as_uint(__uint_as_float(o.x) + __uint_as_float(v[b][4 * i])),
-                                           __float_as_uint(__uint_as_float(o.y) + __uint_as_float(v[b][4 * i + 1])),
-                                           __float_as_uint(__uint_as_float(o.z) + __uint_as_float(v[b][4 * i + 2])),
-                                           __float_as_uint(__uint_as_float(o.w) + __uint_as_float(v[b][4 * i + 3]))));
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(&tma_o, ring + slot * WBOX, ocol + 32 * b, orow);
-                    ptx::bulk_commit_group();
-                }
-                if constexpr (kWgRedMask != 0) {
-                    // box b + 1 goes by reduce-add, staged in this slot once
-                    // the store has read it
-                    if (lane == 0)
+                    if constexpr (MIX) {
+                        // box b + 1 goes by reduce-add, staged in this slot once
+                        // the store has read it
+                        if (lane == 0)
+                            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        __syncwarp();
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            ptx::sts128(box + ptx::swz128(lane, i),
+                                        make_uint4(v[b + 1][4 * i], v[b + 1][4 * i + 1], v[b + 1][4 * i + 2],
+                                                   v[b + 1][4 * i + 3]));
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * (b + 1), orow);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    // refill the slot with the load-add-store box WS further on,
+                    // once what was staged in it has been read
+                    if (lane == 0 && (j + WS < NR || nxt >= 0)) {
                         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        ptx::sts128(box + ptx::swz128(lane, i),
-                                    make_uint4(v[b + 1][4 * i], v[b + 1][4 * i + 1], v[b + 1][4 * i + 2],
-                                               v[b + 1][4 * i + 3]));
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_reduce_add_2d(&tma_o, ring + slot * WBOX, ocol + 32 * (b + 1), orow);
-                        ptx::bulk_commit_group();
+                        if (j + WS < NR)
+                            issue_load(slot, ocol + 32 * rmw_pos(j + WS), orow);
+                        else
+                            issue_load(slot, ncol + 32 * rmw_pos(j + WS - NR), nrow);
                     }
                 }
-                // refill the slot with the load-add-store box WS further on,
-                // once what was staged in it has been read
-                if (lane == 0 && (j + WS < NR || nxt >= 0)) {
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    if (j + WS < NR)
-                        issue_load(slot, ocol + 32 * rmw_pos(j + WS), orow);
-                    else
-                        issue_load(slot, ncol + 32 * rmw_pos(j + WS - NR), nrow);
-                }
+                cur = nxt;
             }
-            cur = nxt;
+        };
+        // skewed splits: the largest group against the mean live group
+        int32_t mmax = 0, live = 0;
+        for (int g = lane; g < p.G; g += 32) {
+            const int32_t m = c.s_off[g + 1] - c.s_off[g];
+            mmax = max(mmax, m);
+            live += m > 0;
         }
+        mmax = __reduce_max_sync(0xffffffffu, mmax);
+        live = __reduce_add_sync(0xffffffffu, live);
+        const bool mix = acc && (int64_t)mmax * live >= kWgMixSkew * (int64_t)c.s_off[p.G];
+        if (mix)
+            epilogue(std::integral_constant<bool, true>{});
+        else
+            epilogue(std::integral_constant<bool, false>{});
         if (lane == 0) {
             // loads still in flight (an abort) land before the CTA leaves
             volatile int no_abort = 0;

@@ -239,6 +239,36 @@ def test_wgrad_accumulate_and_empty_groups():
     assert np.all(fresh[0] == 0) and not np.any(np.signbit(fresh[0]))
 
 
+@pytest.mark.parametrize("splits", [
+    [1536, 32, 0, 64, 32, 96],       # skewed: boxes 1 and 3 of each warp's share go by reduce-add
+    [352, 320, 0, 288, 352, 320],    # even: every box by load + add + store
+])
+def test_wgrad_accumulate_skewed_and_even_splits(splits):
+    """The accumulating wide wgrad (k % 256 == 0) adds its tiles into the main
+    grad by two routes, chosen on the device from the split sizes: with
+    skewed splits half of each warp's boxes go by TMA reduce-add, with even
+    splits all by load + add + store.  Both match the oracle per group, give
+    the same bits with the run-time and the static tile order, and leave an
+    empty group bit-unchanged."""
+    splits = np.array(splits, np.int32)
+    G, N, K = len(splits), 256, 512
+    L = int(splits.sum())
+    dy = np.concatenate([W.normal_bf16((L, N), 16), W.uniform_bf16((64, N), 17, -4, 4)])
+    x = np.concatenate([W.normal_bf16((L, K), 18), W.uniform_bf16((64, K), 19, -4, 4)])
+    init = np.random.default_rng(20).standard_normal((G, N, K)).astype(np.float32)
+    got = gpu_wgrad(dy, x, splits, G, N, K, accumulate=True, init=init)
+    static = gpu_wgrad(dy, x, splits, G, N, K, accumulate=True, init=init, workspace=None)
+    np.testing.assert_array_equal(got.view(np.uint32), static.view(np.uint32))
+    np.testing.assert_array_equal(got[2], init[2])
+    want = ora_wgrad(dy, x, splits, G, N, K, True, init)
+    for g in range(G):
+        if splits[g]:
+            inc, ref = got[g].astype(np.float64) - init[g], want[g] - init[g]
+            slack = 2.0 ** -24 * np.abs(got[g].astype(np.float64))
+            resid = np.maximum(np.abs(inc - ref) - slack, 0.0)
+            assert np.linalg.norm(resid) <= REL_TOL * np.linalg.norm(ref), f"group {g}"
+
+
 def test_wgrad_empty_buffer_zero_fill():
     G, N, K = 3, 128, 128
     st = status_dev()
