@@ -352,8 +352,8 @@ gq_status gq_gemm_dgrad(const gq_quantized* dy, const gq_quantized* w,
  *           GQ_WGRAD_WORKSPACE_BYTES bytes, 16-byte aligned, that the call
  *           clears on `stream` before its kernel (cudaMemsetAsync) and uses
  *           as tile-claim counters.  With a workspace the MX wgrad hands out
- *           its output tiles at run time: half of the CTAs take tiles of the
- *           groups in decreasing order of m_g, the other half in increasing
+ *           its output tiles at run time: 40% of the CTAs take tiles of the
+ *           groups in decreasing order of m_g, the others in increasing
  *           order, until the two meet, so the long contractions of the
  *           largest groups overlap the main-grad traffic of the smallest
  *           (with skewed splits every CTA would otherwise work through the

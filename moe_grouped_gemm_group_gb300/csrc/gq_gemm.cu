@@ -144,7 +144,7 @@ constexpr int64_t kWgMixSkew = GQ_WG_MIX_SKEW;
 // groups down in the run-time order; the others start from the smallest
 // (tuning knob).
 #ifndef GQ_WG_FRONT_PCT
-#define GQ_WG_FRONT_PCT 50
+#define GQ_WG_FRONT_PCT 40
 #endif
 constexpr int kWgFrontPct = GQ_WG_FRONT_PCT;
 
@@ -465,77 +465,88 @@ __device__ __forceinline__ uint32_t warp_colmax(const uint32_t (&x)[32], int lan
     return max(b0 ? m[1] : m[0], __shfl_xor_sync(0xffffffffu, b0 ? m[0] : m[1], 1));
 }
 
-// The fused activation of one epilogue warp: its 32 rows (lane = row, one
-// 32-row block of the group) x 128 columns of the fp32 result in v.
-// a = probs[r] * relu(y)^2 in fp32 (t = max(y, 0); t = t * t; a = t * p),
-// then MXFP8 1x32 codes and E8M0 scales of a, rowwise (blocks of 32 columns)
-// and columnwise (the warp's 32 rows), written to the grouped layout of a
-// [R, n] buffer: atoms of group g at 512 * (n/128) * (tiles before g),
-// rowwise [row tile][column block], columnwise [column block][row tile],
-// byte (r % 32) * 16 + (r / 32) * 4 + j.  A warp whose rows lie past the
-// group's end writes the zero entries of its atoms and nothing else.
-template <int BN>
-__device__ __forceinline__ void act_quant_warp(const GemmArgs& p, const Tile& t, const int32_t* s_tp, int q,
-                                               int h, int lane, bool live, uint32_t (&v)[4][32])
+// The fused ScaledSReLU of one epilogue warp: its 32 rows (lane = row, one
+// 32-row block of the group) x 128 columns of the fp32 result, one 32-column
+// chunk at a time.  a = probs[r] * relu(y)^2 in fp32 (t = max(y, 0); t = t *
+// t; a = t * p), then MXFP8 1x32 codes and E8M0 scales of a, rowwise (blocks
+// of 32 columns) and columnwise (the warp's 32 rows), written to the grouped
+// layout of a [R, n] buffer: atoms of group g at 512 * (n/128) * (tiles
+// before g), rowwise [row tile][column block], columnwise [column
+// block][row tile], byte (r % 32) * 16 + (r / 32) * 4 + j.
+
+// Where one warp's activation scale bytes go.
+struct ActAtoms {
+    uint8_t* row;     // this lane's 32-bit word (or 16-bit half) of the rowwise atom
+    uint8_t* col;     // this lane's first byte of the columnwise atom
+};
+
+// Atoms of the activation columns [c0, c0 + 128) of tile t (SReLU: c0 =
+// col0 + 128 h of the [R, n] buffer; SwiGLU: the 128-column block holding the
+// warp's 64 columns of the [R, n/2] buffer), for rows 32 q + lane.
+__device__ __forceinline__ ActAtoms act_atoms(const GemmArgs& p, const Tile& t, const int32_t* s_tp, int64_t width,
+                                              int64_t c0, int q, int lane)
 {
-    const int64_t nb = p.n / 128;
-    const int64_t cb = (t.col0 + 128 * h) / 128;
+    const int64_t nb = width / 128;
+    const int64_t cb = c0 / 128;
     const int64_t sb = 512 * nb * (int64_t)s_tp[t.g];
-    uint8_t* ratom = p.act_row_scale + sb + (t.mt * nb + cb) * 512;
-    uint8_t* catom = p.act_col_scale + sb + (cb * t.T + t.mt) * 512;
-    if (!live) {
-        *reinterpret_cast<uint32_t*>(ratom + lane * 16 + q * 4) = 0u;
+    ActAtoms a;
+    a.row = p.act_row_scale + sb + (t.mt * nb + cb) * 512 + lane * 16 + q * 4;
+    a.col = p.act_col_scale + sb + (cb * t.T + t.mt) * 512 + lane * 16 + q;
+    return a;
+}
+
+// MX codes of one 32-column block x of the warp's rows (lane = row) into
+// row `row`, columns [col, col + 32) of the rowwise and columnwise code
+// buffers of width `width`; the column scale byte goes to *cbyte, the row
+// scale byte is returned.
+__device__ __forceinline__ uint32_t act_block_codes(const GemmArgs& p, int64_t row, int64_t col, int64_t width,
+                                                    uint32_t amax_r, uint8_t* cbyte_at, int lane,
+                                                    const uint32_t (&x)[32])
+{
+    const uint32_t rb = e8m0_of_f32(__uint_as_float(amax_r));
+    const float rs = inv_scale_of(rb);
+    {
+        uint32_t w[8];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            catom[lane * 16 + cc * 4 + q] = 0;
-        return;
+        for (int i = 0; i < 8; ++i)
+            w[i] = codes4(__uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]), __uint_as_float(x[4 * i + 2]),
+                          __uint_as_float(x[4 * i + 3]), rs, rs, rs, rs);
+        uint4* dst = reinterpret_cast<uint4*>(p.act_row + row * width + col);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    const int64_t row = t.row0 + 32 * q + lane;
-    const float pr = __ldg(p.act_probs + row);
-    uint32_t rword = 0;
+    const uint32_t cbyte = e8m0_of_f32(__uint_as_float(warp_colmax(x, lane)));
+    *cbyte_at = (uint8_t)cbyte;
+    const float csc = inv_scale_of(cbyte);
+    {
+        uint32_t w[8];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int64_t col = t.col0 + 128 * h + 32 * cc;
-        uint32_t amax_r = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            float x = __uint_as_float(v[cc][i]);
-            x = x > 0.f ? x : 0.f;
-            const float a = __fmul_rn(__fmul_rn(x, x), pr);
-            v[cc][i] = __float_as_uint(a);
-            amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
-        }
-        // rowwise
-        const uint32_t rb = e8m0_of_f32(__uint_as_float(amax_r));
-        const float rs = inv_scale_of(rb);
-        rword |= rb << (8 * cc);
-        {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
-                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]), rs, rs, rs, rs);
-            uint4* dst = reinterpret_cast<uint4*>(p.act_row + row * p.n + col);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(warp_colmax(v[cc], lane)));
-        catom[lane * 16 + cc * 4 + q] = (uint8_t)cbyte;
-        const float csc = inv_scale_of(cbyte);
-        {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
-                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]),
-                              __shfl_sync(0xffffffffu, csc, 4 * i), __shfl_sync(0xffffffffu, csc, 4 * i + 1),
-                              __shfl_sync(0xffffffffu, csc, 4 * i + 2), __shfl_sync(0xffffffffu, csc, 4 * i + 3));
-            uint4* dst = reinterpret_cast<uint4*>(p.act_col + row * p.n + col);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
+        for (int i = 0; i < 8; ++i)
+            w[i] = codes4(__uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]), __uint_as_float(x[4 * i + 2]),
+                          __uint_as_float(x[4 * i + 3]), __shfl_sync(0xffffffffu, csc, 4 * i),
+                          __shfl_sync(0xffffffffu, csc, 4 * i + 1), __shfl_sync(0xffffffffu, csc, 4 * i + 2),
+                          __shfl_sync(0xffffffffu, csc, 4 * i + 3));
+        uint4* dst = reinterpret_cast<uint4*>(p.act_col + row * width + col);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    *reinterpret_cast<uint32_t*>(ratom + lane * 16 + q * 4) = rword;
+    return rb;
+}
+
+// ScaledSReLU of chunk x (in place), then its codes; returns the row scale byte.
+__device__ __forceinline__ uint32_t act_srelu_chunk(const GemmArgs& p, int64_t row, int64_t col, float pr,
+                                                    uint8_t* cbyte_at, int lane, uint32_t (&x)[32])
+{
+    uint32_t amax_r = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float y = __uint_as_float(x[i]);
+        y = y > 0.f ? y : 0.f;
+        const float a = __fmul_rn(__fmul_rn(y, y), pr);
+        x[i] = __float_as_uint(a);
+        amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
+    }
+    return act_block_codes(p, row, col, p.n, amax_r, cbyte_at, lane, x);
 }
 
 // exp for the fused ScaledSwiGLU, this library's own: the argument clamped
@@ -564,76 +575,24 @@ __device__ __forceinline__ float act_exp(float x)
 // silu(x) = x / (1 + exp(-x)), fp32 op by op.
 __device__ __forceinline__ float act_silu(float x) { return __fdiv_rn(x, __fadd_rn(1.f, act_exp(-x))); }
 
-// The fused ScaledSwiGLU of one epilogue warp: its 32 rows (lane = row, one
-// 32-row block of the group), gate columns in v[0], v[1] and the matching
-// linear columns in v[2], v[3] -- output columns [gc + 64 h, gc + 64 h + 64)
-// of the [R, act_half] activation, gc = col0 / 2.  a = (silu(g) * l) *
-// probs[r] in fp32 op by op, then MXFP8 1x32 codes and E8M0 scales rowwise
-// (2 blocks of 32 columns: bytes 2 h, 2 h + 1 of the row's atom word) and
-// columnwise (the warp's 32 rows) into the grouped layout of the [R,
-// act_half] buffer.  A warp whose rows lie past the group's end writes the
-// zero entries of its atoms and nothing else.
-__device__ __forceinline__ void act_glu_warp(const GemmArgs& p, const Tile& t, const int32_t* s_tp, int q, int h,
-                                             int lane, bool live, uint32_t (&v)[4][32])
+// The fused ScaledSwiGLU of one epilogue warp, one 32-column output block at
+// a time: gate columns g and the matching linear columns l of its 32 rows
+// (lane = row, one 32-row block of the group).  a = (silu(g) * l) * probs[r]
+// in fp32 op by op (into g), then MXFP8 1x32 codes and E8M0 scales of a,
+// rowwise and columnwise, at output columns [col, col + 32) of the [R,
+// act_half] buffer; returns the row scale byte.
+__device__ __forceinline__ uint32_t act_glu_chunk(const GemmArgs& p, int64_t row, int64_t col, float pr,
+                                                  uint8_t* cbyte_at, int lane, uint32_t (&g)[32],
+                                                  const uint32_t (&l)[32])
 {
-    const int64_t nb = p.act_half / 128;
-    const int64_t gc = t.col0 / 2;
-    const int64_t cb = gc / 128;
-    const int64_t sb = 512 * nb * (int64_t)s_tp[t.g];
-    uint8_t* ratom = p.act_row_scale + sb + (t.mt * nb + cb) * 512;
-    uint8_t* catom = p.act_col_scale + sb + (cb * t.T + t.mt) * 512;
-    uint16_t* rword_at = reinterpret_cast<uint16_t*>(ratom + lane * 16 + q * 4 + 2 * h);
-    if (!live) {
-        *rword_at = 0;
+    uint32_t amax_r = 0;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
-            catom[lane * 16 + (2 * h + cc) * 4 + q] = 0;
-        return;
+    for (int i = 0; i < 32; ++i) {
+        const float a = __fmul_rn(__fmul_rn(act_silu(__uint_as_float(g[i])), __uint_as_float(l[i])), pr);
+        g[i] = __float_as_uint(a);
+        amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
     }
-    const int64_t row = t.row0 + 32 * q + lane;
-    const float pr = __ldg(p.act_probs + row);
-    uint32_t rword = 0;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int64_t col = gc + 64 * h + 32 * cc;
-        uint32_t amax_r = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float a = __fmul_rn(__fmul_rn(act_silu(__uint_as_float(v[cc][i])), __uint_as_float(v[cc + 2][i])),
-                                      pr);
-            v[cc][i] = __float_as_uint(a);
-            amax_r = max(amax_r, __float_as_uint(a) & 0x7fffffffu);
-        }
-        const uint32_t rb = e8m0_of_f32(__uint_as_float(amax_r));
-        const float rs = inv_scale_of(rb);
-        rword |= rb << (8 * cc);
-        {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
-                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]), rs, rs, rs, rs);
-            uint4* dst = reinterpret_cast<uint4*>(p.act_row + row * p.act_half + col);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-        const uint32_t cbyte = e8m0_of_f32(__uint_as_float(warp_colmax(v[cc], lane)));
-        catom[lane * 16 + (2 * h + cc) * 4 + q] = (uint8_t)cbyte;
-        const float csc = inv_scale_of(cbyte);
-        {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = codes4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
-                              __uint_as_float(v[cc][4 * i + 2]), __uint_as_float(v[cc][4 * i + 3]),
-                              __shfl_sync(0xffffffffu, csc, 4 * i), __shfl_sync(0xffffffffu, csc, 4 * i + 1),
-                              __shfl_sync(0xffffffffu, csc, 4 * i + 2), __shfl_sync(0xffffffffu, csc, 4 * i + 3));
-            uint4* dst = reinterpret_cast<uint4*>(p.act_col + row * p.act_half + col);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-    }
-    *rword_at = (uint16_t)rword;
+    return act_block_codes(p, row, col, p.act_half, amax_r, cbyte_at, lane, g);
 }
 
 // Wait for the TMA writes of the last min(stages, issued) issued stages, so
@@ -1296,16 +1255,33 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
             if (lane == 0)
                 ptx::mbar_arrive(&c.tempty[0]);
             ++tiles_done;
+            // the activation's scale atoms (SwiGLU: the [R, n / 2] buffer's
+            // 128-column block holding the warp's 64 columns gc + 64 h)
+            ActAtoms at{};
+            if constexpr (ACT == 1)
+                at = act_atoms(p, t, c.s_tp, p.n, t.col0 + 128 * h, q, lane);
+            if constexpr (ACT == 2)
+                at = act_atoms(p, t, c.s_tp, p.act_half, gc, q, lane);
             if (32 * q >= t.rows) {
-                if constexpr (ACT == 1)
-                    act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, false, v);
-                if constexpr (ACT == 2)
-                    act_glu_warp(p, t, c.s_tp, q, h, lane, false, v);
+                // rows past the group's end: only the zero entries of the atoms
+                if constexpr (ACT == 1) {
+                    *reinterpret_cast<uint32_t*>(at.row) = 0u;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        at.col[cc * 4] = 0;
+                }
+                if constexpr (ACT == 2) {
+                    *reinterpret_cast<uint16_t*>(at.row + 2 * h) = 0;
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+                        at.col[(2 * h + cc) * 4] = 0;
+                }
                 continue;
             }
             const int32_t orow = (int32_t)(t.row0 + 32 * q);
-#pragma unroll
-            for (int b = 0; b < NBOX; ++b) {
+            // box b of the warp's output (bf16: TMEM chunk b; fp32: half b & 1
+            // of chunk b >> 1) through the warp's staging box
+            auto store_box = [&](int b) {
                 // bias of the box's columns, added just before they are converted
                 if (KIND == GEMM_FPROP && p.bias && (OUT_BF16 || (b & 1) == 0))
                     add_bias32(p, t.g, y_col(OUT_BF16 ? b : b >> 1), v[OUT_BF16 ? b : b >> 1]);
@@ -1337,11 +1313,45 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     ptx::tma_store_2d(&tma_o, box, OUT_BF16 ? y_col(b) : y_col(b >> 1) + 16 * (b & 1), orow);
                     ptx::bulk_commit_group();
                 }
+            };
+            // the pre-activation Y of TMEM chunk cc
+            auto store_chunk = [&](int cc) {
+                if (OUT_BF16) {
+                    store_box(cc);
+                } else {
+                    store_box(2 * cc);
+                    store_box(2 * cc + 1);
+                }
+            };
+            if constexpr (ACT == 0) {
+#pragma unroll
+                for (int b = 0; b < NBOX; ++b)
+                    store_box(b);
+            } else {
+                // chunk by chunk: Y, then the activation's codes and scales,
+                // so that a chunk's registers are free once it is done
+                const int64_t row = t.row0 + 32 * q + lane;
+                const float pr = __ldg(p.act_probs + row);
+                uint32_t rword = 0;
+                if constexpr (ACT == 1) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        store_chunk(cc);
+                        rword |= act_srelu_chunk(p, row, t.col0 + 128 * h + 32 * cc, pr, at.col + cc * 4, lane,
+                                                 v[cc]) << (8 * cc);
+                    }
+                    *reinterpret_cast<uint32_t*>(at.row) = rword;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        store_chunk(j);
+                        store_chunk(j + 2);
+                        rword |= act_glu_chunk(p, row, gc + 64 * h + 32 * j, pr, at.col + (2 * h + j) * 4, lane, v[j],
+                                               v[j + 2]) << (8 * j);
+                    }
+                    *reinterpret_cast<uint16_t*>(at.row + 2 * h) = (uint16_t)rword;
+                }
             }
-            if constexpr (ACT == 1)
-                act_quant_warp<BN>(p, t, c.s_tp, q, h, lane, true, v);
-            if constexpr (ACT == 2)
-                act_glu_warp(p, t, c.s_tp, q, h, lane, true, v);
         }
         if (lane == 0)
             ptx::bulk_wait_all();
