@@ -26,7 +26,10 @@
  *  - Every call is asynchronous on `stream` (NULL = the legacy default
  *    stream) and never synchronises with the host, so a sequence of calls
  *    can be captured in a CUDA graph once each (device, shape) pair has been
- *    called once outside capture.
+ *    called once outside capture.  That first call's set-up (kernel
+ *    attributes) is cached per CUDA context: after cudaDeviceReset, or in
+ *    another context, the next call redoes it, and it too must come before
+ *    any capture.
  *  - Buffers are row-major.  A token buffer has rows_cap rows R; group g
  *    owns rows [o_g, o_g + m_g) with o_g = m_0 + ... + m_{g-1} and
  *    L = sum(m_g) <= R.  Rows >= L are padding: never read, never written,

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
 
 #include "gq_internal.h"
@@ -13,30 +14,58 @@ namespace gq {
 
 const DeviceInfo& device_info()
 {
-    static DeviceInfo infos[64];
-    static std::once_flag flags[64];
+    // one entry per device ordinal, filled on first use (node addresses stay
+    // valid as the map grows)
+    static std::mutex mu;
+    static std::map<int, DeviceInfo> infos;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
         dev = 0;
-    std::call_once(flags[dev], [dev] {
-        DeviceInfo& d = infos[dev];
-        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
-        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
-        int optin = 0;
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        d.smem_optin = (size_t)optin;
-        if (d.sm_count <= 0)
-            d.sm_count = 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = infos.find(dev);
+    if (it != infos.end())
+        return it->second;
+    DeviceInfo d;
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.smem_optin = (size_t)optin;
+    if (d.sm_count <= 0)
+        d.sm_count = 1;
+    return infos.emplace(dev, d).first->second;
+}
+
+bool current_context_id(unsigned long long* id)
+{
+    using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+    using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PfnCtxGetCurrent>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PfnCtxGetId>(p);
     });
-    return infos[dev];
+    if (!get_current || !get_id)
+        return false;
+    CUcontext ctx = nullptr;
+    return get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
 }
 
 cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* blocks_per_sm)
 {
     struct Entry {
         const void* fn;
-        int dev, dyn_smem, threads, per_sm;
+        unsigned long long ctx;
+        int dyn_smem, threads, per_sm;
     };
     static std::mutex mu;
     static Entry cache[256];
@@ -44,10 +73,17 @@ cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* block
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return cudaErrorInvalidDevice;
+    // a runtime call that makes the device's primary context current when
+    // no context is yet (the first call of a process)
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) {
+        if (cudaSetDevice(dev) != cudaSuccess || !current_context_id(&ctx))
+            return cudaErrorInvalidDevice;
+    }
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i) {
         const Entry& e = cache[i];
-        if (e.fn == fn && e.dev == dev && e.dyn_smem == dyn_smem && e.threads == threads) {
+        if (e.fn == fn && e.ctx == ctx && e.dyn_smem == dyn_smem && e.threads == threads) {
             if (blocks_per_sm)
                 *blocks_per_sm = e.per_sm;
             return cudaSuccess;
@@ -68,7 +104,7 @@ cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* block
             n = 1;
     }
     if (used < 256)
-        cache[used++] = Entry{fn, dev, dyn_smem, threads, n};
+        cache[used++] = Entry{fn, ctx, dyn_smem, threads, n};
     if (blocks_per_sm)
         *blocks_per_sm = n;
     return cudaSuccess;

@@ -20,7 +20,14 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();
 
-// Per (kernel, device) set-up, done on the first launch there and cached:
+// The driver's ID of the current CUDA context (never reused within a
+// process), false while no context is current.  Per-context set-up (kernel
+// attributes, symbol addresses) is cached under it, so that a new context --
+// another one on the same device, or the one after cudaDeviceReset -- gets
+// its own set-up.
+bool current_context_id(unsigned long long* id);
+
+// Per (kernel, context) set-up, done on the first launch there and cached:
 // the dynamic shared-memory limit and the resident blocks per SM.  Later
 // launches only enqueue work.
 cudaError_t prepare_kernel(const void* fn, int dyn_smem, int threads, int* blocks_per_sm);

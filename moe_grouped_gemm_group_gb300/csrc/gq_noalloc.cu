@@ -9,8 +9,6 @@
 // call made with that context current, and handed to the regular entry point
 // as its workspace.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,38 +34,12 @@ struct Entry {
 std::mutex g_mu;
 std::vector<Entry> g_addr;
 
-using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
-using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
-
-// The current context's ID from the driver (taken at run time, like the
-// tensor-map encoder, so that loading the library needs no GPU).
-bool current_context_id(unsigned long long* id)
-{
-    static PfnCtxGetCurrent get_current = nullptr;
-    static PfnCtxGetId get_id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<PfnCtxGetCurrent>(p);
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<PfnCtxGetId>(p);
-    });
-    if (!get_current || !get_id)
-        return false;
-    CUcontext ctx = nullptr;
-    return get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 // Device address of the scratch array in the current context (looked up on
 // the first call there), or nullptr with *err set.
 void* scratch_address(gq_status* err)
 {
     unsigned long long id = 0;
-    const bool have_id = current_context_id(&id);     // false while no context is current
+    const bool have_id = gq::current_context_id(&id);     // false while no context is current
     if (have_id) {
         std::lock_guard<std::mutex> lock(g_mu);
         for (const Entry& e : g_addr)
@@ -81,7 +53,7 @@ void* scratch_address(gq_status* err)
         *err = GQ_ERR_CUDA;
         return nullptr;
     }
-    if (!have_id && !current_context_id(&id)) {
+    if (!have_id && !gq::current_context_id(&id)) {
         *err = GQ_ERR_CUDA;
         return nullptr;
     }

@@ -6,18 +6,23 @@
  * describes the grouped tensors with gq_quantized, and runs the MXFP8
  * quantisation of X and W, the grouped fprop and the k-grouped wgrad, plus
  * two calls that must be refused on the host.  Results go to raw files for
- * the test to compare with the oracle.
+ * the test to compare with the oracle.  Then it resets the device
+ * (cudaDeviceReset: the library's per-context set-up and the no-alloc
+ * wgrad's array address must be redone in the new context), allocates and
+ * quantises again, and checks that the no-alloc wgrad gives the same bits.
  *
  * usage: c_abi_check DIR G R K N
  *   DIR/splits.bin  int32[G]          DIR/x.bin  uint16[R][K]  (bf16 bits)
  *   DIR/w.bin       uint16[G*N][K]    DIR/dy.bin uint16[R][N]
  * writes DIR/y.bin (float[R][N]), DIR/dw.bin (float[G][N][K]),
  *        DIR/xrow.bin (uint8[R][K] rowwise codes), DIR/status.txt
+ *        ("status refused_cols refused_shape reset_status reset_equal")
  */
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "gq.h"
 
@@ -164,11 +169,46 @@ int main(int argc, char** argv)
         write_file(dir, "dw.bin", h_dw, sizeof(float) * (size_t)(G * N * K)) ||
         write_file(dir, "xrow.bin", h_xrow, (size_t)(R * K)))
         return 5;
-    snprintf(path, sizeof path, "%s/status.txt", dir);
-    f = fopen(path, "w");
-    if (!f)
-        return 5;
-    fprintf(f, "%d %d %d\n", (int)h_status, (int)refused_cols, (int)refused_shape);
-    fclose(f);
+
+    /* a new context: everything again, the no-alloc wgrad must give the same bits */
+    CHECK_CUDA(cudaDeviceReset());
+    CHECK_CUDA(cudaStreamCreate(&stream));
+    CHECK_CUDA(cudaMalloc((void**)&d_splits, sizeof(int32_t) * (size_t)G));
+    CHECK_CUDA(cudaMalloc((void**)&d_status, sizeof(int32_t)));
+    CHECK_CUDA(cudaMalloc(&d_x, 2 * (size_t)(R * K)));
+    CHECK_CUDA(cudaMalloc(&d_dy, 2 * (size_t)(R * N)));
+    CHECK_CUDA(cudaMalloc((void**)&d_dw, sizeof(float) * (size_t)(G * N * K)));
+    CHECK_CUDA(cudaMemcpyAsync(d_splits, h_splits, sizeof(int32_t) * (size_t)G, cudaMemcpyHostToDevice, stream));
+    CHECK_CUDA(cudaMemcpyAsync(d_x, h_x, 2 * (size_t)(R * K), cudaMemcpyHostToDevice, stream));
+    CHECK_CUDA(cudaMemcpyAsync(d_dy, h_dy, 2 * (size_t)(R * N), cudaMemcpyHostToDevice, stream));
+    CHECK_CUDA(cudaMemsetAsync(d_status, 0, sizeof(int32_t), stream));
+    if (alloc_mx(&qx, G, R, K) || alloc_mx(&qdy, G, R, N)) {
+        fprintf(stderr, "cudaMalloc of the quantised buffers failed after the reset\n");
+        return 2;
+    }
+    CHECK_GQ(gq_quantize(d_x, R, K, d_splits, G, &mx, &qx, d_status, (gq_stream_t)stream));
+    CHECK_GQ(gq_quantize(d_dy, R, N, d_splits, G, &mx, &qdy, d_status, (gq_stream_t)stream));
+    CHECK_GQ(gq_gemm_wgrad_noalloc(&qdy, &qx, d_splits, G, N, K, d_dw, 0, d_status, (gq_stream_t)stream));
+    {
+        float* h_dw2 = (float*)malloc(sizeof(float) * (size_t)(G * N * K));
+        int32_t h_status2 = 0;
+        int equal = 1;
+        size_t i;
+        CHECK_CUDA(cudaMemcpyAsync(h_dw2, d_dw, sizeof(float) * (size_t)(G * N * K), cudaMemcpyDeviceToHost, stream));
+        CHECK_CUDA(cudaMemcpyAsync(&h_status2, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
+        CHECK_CUDA(cudaStreamSynchronize(stream));
+        for (i = 0; i < (size_t)(G * N * K); ++i)
+            if (memcmp(&h_dw2[i], &h_dw[i], sizeof(float)) != 0) {
+                equal = 0;
+                break;
+            }
+        snprintf(path, sizeof path, "%s/status.txt", dir);
+        f = fopen(path, "w");
+        if (!f)
+            return 5;
+        fprintf(f, "%d %d %d %d %d\n", (int)h_status, (int)refused_cols, (int)refused_shape, (int)h_status2, equal);
+        fclose(f);
+        free(h_dw2);
+    }
     return 0;
 }

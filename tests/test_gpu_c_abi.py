@@ -3,7 +3,10 @@ torch: tests/c_abi_check.c is built with gcc against include/gq.h, linked to
 libgq.so and the CUDA runtime, and run in its own process.  It allocates its
 device buffers with cudaMalloc, quantises X, W and dY (MXFP8), runs the
 grouped fprop and the k-grouped wgrad, and checks two host-side refusals;
-its outputs are compared here with the oracle."""
+its outputs are compared here with the oracle.  It then resets the device
+(cudaDeviceReset), so that the library meets a new CUDA context: its cached
+per-context set-up (kernel attributes, the no-alloc wgrad's array address)
+must be redone there, and the no-alloc wgrad must give the same bits."""
 import os
 import subprocess
 
@@ -56,8 +59,11 @@ def test_c_program_quantize_fprop_wgrad(tmp_path):
     dy.tofile(tmp_path / "dy.bin")
     subprocess.run([str(exe), str(tmp_path), str(G), str(R), str(K), str(N)], check=True, timeout=300)
 
-    status, refused_cols, refused_shape = (int(v) for v in (tmp_path / "status.txt").read_text().split())
+    status, refused_cols, refused_shape, reset_status, reset_equal = (
+        int(v) for v in (tmp_path / "status.txt").read_text().split())
     assert status == 0
+    assert reset_status == 0, "device status after cudaDeviceReset"
+    assert reset_equal == 1, "the no-alloc wgrad changed after cudaDeviceReset"
     assert refused_cols == -2            # GQ_ERR_ALIGNMENT: cols % 128
     assert refused_shape == -7           # GQ_ERR_SHAPE_MISMATCH: descriptor cols
     xrow = np.fromfile(tmp_path / "xrow.bin", np.uint8).reshape(R, K)
