@@ -977,10 +977,10 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                         break;
                     ptx::tc_fence_after_sync();
                     const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
-    #pragma unroll
+#pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
                         ptx::tmem_ld_32x32(tb + 32 * cc, v[cc]);
-    #pragma unroll
+#pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
                         ptx::tmem_wait_ld(v[cc]);
                     ptx::tc_fence_before_sync();
@@ -989,9 +989,9 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                         ptx::mbar_arrive(&c.tempty[0]);
                     ++tiles_done;
                 } else {                                      // empty group, accumulate = 0: dW_g = 0
-    #pragma unroll
+#pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i)
                             v[cc][i] = 0u;
                 }
@@ -1006,7 +1006,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     ncol = box_col(tn, 0);
                 }
                 if (!acc) {
-    #pragma unroll
+#pragma unroll
                     for (int b = 0; b < 4; ++b, ++boxes) {
                         const int slot = (int)(boxes % (uint32_t)WS);
                         const uint32_t box = ring_addr + slot * WBOX;
@@ -1017,7 +1017,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                                 asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
                         }
                         __syncwarp();
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 8; ++j)
                             ptx::sts128(box + ptx::swz128(lane, j),
                                         make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]));
@@ -1031,7 +1031,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     cur = nxt;
                     continue;
                 }
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < NR; ++j, ++boxes) {
                     const int b = rmw_pos(j);
                     const int slot = (int)(boxes % (uint32_t)WS);
@@ -1042,7 +1042,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                     }
                     lph ^= 1u << slot;
                     lpend &= ~(1u << slot);
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint4 o = ptx::lds128(box + ptx::swz128(lane, i));
                         ptx::sts128(box + ptx::swz128(lane, i),
@@ -1063,7 +1063,7 @@ k_gemm_mx(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUt
                         if (lane == 0)
                             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                         __syncwarp();
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 8; ++i)
                             ptx::sts128(box + ptx::swz128(lane, i),
                                         make_uint4(v[b + 1][4 * i], v[b + 1][4 * i + 1], v[b + 1][4 * i + 2],
