@@ -169,3 +169,60 @@ def test_fused_swiglu_shape_checks():
     wrong = gq.alloc_quantized(128, 512, 1, mx_recipe(True, True), DEV)      # must be n / 2 = 256 wide
     with pytest.raises(gq.GQError, match="GQ_ERR_SHAPE_MISMATCH"):
         gq.gq_gemm_fprop_swiglu_quant(xq, wq, splits_dev(splits), 1, 512, 256, probs, y, gq.DTYPE_F32, wrong, st)
+
+
+# --------------------------------------------------------------------------- #
+# full size: moe_e64_zipf fc1 in the bench's launch configuration             #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("act_kind", ["srelu", "swiglu"])
+def test_fused_activation_moe_e64_zipf_fc1(act_kind):
+    """E = 64, hidden 7168, 65536 Zipf-routed tokens + 1024 garbage rows, fc1
+    width 2048 (ScaledSReLU) or 2 x 2048 (ScaledSwiGLU): the fused kernel's
+    fp32 Y equals the plain fprop's bit for bit (same tiles, same contraction
+    order; the plain fprop is held to the oracle at these shapes in
+    test_gpu_fullsize.py), and the activation's codes and scale regions equal
+    the oracle's ScaledSReLU / ScaledSwiGLU + MX quantisation of that Y, byte
+    for byte, over every live row."""
+    w = W.workload("moe_e64_zipf")
+    E, R, L, K = w.num_groups, w.rows_cap, w.live_rows, w.hidden
+    N = w.ffn if act_kind == "srelu" else 2 * w.ffn
+    x = W.device_activation(w, K, 60, device=DEV)
+    wt = W.device_normal_bf16((E * N, K), w.seed, 0.02, 61, DEV)
+    g = torch.Generator(device=DEV).manual_seed(62)
+    probs = torch.rand(R, generator=g, device=DEV)
+    sp = torch.as_tensor(w.splits).to(DEV)
+    st = status_dev()
+    rec = mx_recipe(True, False)
+    qx = gq.alloc_quantized(R, K, E, rec, DEV)
+    qw = gq.alloc_quantized(E * N, K, E, rec, DEV)
+    gq.gq_quantize(x, sp, E, rec, qx, st)
+    gq.gq_quantize(wt, None, E, rec, qw, st)
+    del x, wt
+    na = N if act_kind == "srelu" else N // 2
+    act = gq.alloc_quantized(R, na, E, mx_recipe(True, True), DEV, fill=0xAB)
+    y = torch.full((R, N), float("nan"), device=DEV)
+    fused = gq.gq_gemm_fprop_srelu_quant if act_kind == "srelu" else gq.gq_gemm_fprop_swiglu_quant
+    fused(qx, qw, sp, E, N, K, probs, y, gq.DTYPE_F32, act, st)
+    y_plain = torch.full((R, N), float("nan"), device=DEV)
+    gq.gq_gemm_fprop(qx, qw, sp, E, N, K, y_plain, gq.DTYPE_F32, st)
+    torch.cuda.synchronize()
+    check_status(st)
+    assert torch.equal(y[:L], y_plain[:L]), "fused Y differs from the plain fprop"
+    assert bool(torch.isnan(y[L:]).all()), "rows past the live total were written"
+
+    yh = host(y[:L])
+    ph = host(probs)
+    yfull = np.zeros((R, N), np.float32)
+    yfull[:L] = yh
+    ref = (O.srelu_quantize_mx if act_kind == "srelu" else O.swiglu_quantize_mx)(yfull, ph, w.splits, E)
+    for name in ("row_data", "col_data"):
+        got = host(getattr(act, name))
+        bad = np.flatnonzero((got[:L] != getattr(ref, name)[:L]).ravel())
+        assert bad.size == 0, f"{name}: {bad.size} codes differ, first at {np.unravel_index(bad[0], (L, na))}"
+        assert np.all(got[L:] == 0xAB), f"{name} written past the live rows"
+    n_scale = len(ref.row_scale)
+    for name in ("row_scale", "col_scale"):
+        got = host(getattr(act, name))
+        assert np.array_equal(got[:n_scale], getattr(ref, name)), name
+        assert np.all(got[n_scale:] == 0xAB), f"{name} written past the grouped extent"
