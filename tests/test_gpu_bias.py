@@ -154,3 +154,63 @@ def test_bias_host_checks():
     ws = torch.empty(gq.gq_dbias_workspace_bytes(1, 128, 256), dtype=torch.uint8, device=DEV)
     with pytest.raises(gq.GQError, match="GQ_ERR_UNSUPPORTED"):
         gq.gq_quantize_dbias(bf16_dev(x), None, 1, ch, qc, db, ws, st)
+
+
+def test_bias_paths_moe_e64_zipf():
+    """moe_e64_zipf sizes (64 experts, 65536 Zipf-routed tokens + 1024
+    garbage rows, hidden 7168, fc1 width 2048).  fprop with a bf16 per-expert
+    bias equals the plain fprop plus the bias bit for bit: the epilogue adds
+    it to the fp32 accumulator once, and the plain fprop is held to the
+    oracle at these shapes in test_gpu_fullsize.py.  The bias gradient fused
+    into the quantisation of a [66560, 7168] dY: codes and scales bitwise
+    equal to gq_quantize's, and 128 sampled columns of every group's column
+    sums against the oracle per group at the GEMMs' tolerance."""
+    w = W.workload("moe_e64_zipf")
+    E, R, L, K, N = w.num_groups, w.rows_cap, w.live_rows, w.hidden, w.ffn
+    splits = np.asarray(w.splits, np.int32)
+    sp = torch.as_tensor(splits).to(DEV)
+    st = status_dev()
+    rec = mx_recipe(True, False)
+    x = W.device_activation(w, K, 80, device=DEV)
+    wt = W.device_normal_bf16((E * N, K), w.seed, 0.02, 81, DEV)
+    b = W.device_normal_bf16((E, N), w.seed, 0.5, 82, DEV)
+    qx = gq.alloc_quantized(R, K, E, rec, DEV)
+    qw = gq.alloc_quantized(E * N, K, E, rec, DEV)
+    gq.gq_quantize(x, sp, E, rec, qx, st)
+    gq.gq_quantize(wt, None, E, rec, qw, st)
+    del x, wt
+    y0 = torch.full((R, N), float("nan"), device=DEV)
+    y1 = torch.full((R, N), float("nan"), device=DEV)
+    gq.gq_gemm_fprop(qx, qw, sp, E, N, K, y0, gq.DTYPE_F32, st)
+    gq.gq_gemm_fprop_bias(qx, qw, sp, E, N, K, b, y1, gq.DTYPE_F32, st)
+    check_status(st)
+    rows_g = torch.repeat_interleave(torch.arange(E, device=DEV), sp.long())
+    want = y0[:L] + b.float()[rows_g]
+    assert torch.equal(y1[:L].view(torch.int32), want.view(torch.int32)), "fprop + bias != fprop, then + bias"
+    assert bool(torch.isnan(y1[L:]).all()), "rows past the live total were written"
+    del qx, qw, y0, y1, want
+
+    dy = W.device_activation(w, K, 83, device=DEV)
+    rec2 = mx_recipe(True, True)
+    q = gq.alloc_quantized(R, K, E, rec2, DEV, fill=0xAB)
+    db = torch.full((E, K), float("nan"), device=DEV)
+    ws = torch.empty(gq.gq_dbias_workspace_bytes(E, R, K), dtype=torch.uint8, device=DEV)
+    gq.gq_quantize_dbias(dy, sp, E, rec2, q, db, ws, st)
+    ref = gq.alloc_quantized(R, K, E, rec2, DEV, fill=0xAB)
+    gq.gq_quantize(dy, sp, E, rec2, ref, st)
+    check_status(st)
+    for name in ("row_data", "col_data"):
+        assert torch.equal(getattr(q, name)[:L], getattr(ref, name)[:L]), name
+    for name in ("row_scale", "col_scale"):
+        assert torch.equal(getattr(q, name), getattr(ref, name)), name
+    cols = np.sort(np.random.default_rng(84).choice(K, 128, replace=False))   # the oracle takes 128-column multiples
+    idx = torch.as_tensor(cols, device=DEV)
+    bits = dy[:L].index_select(1, idx).contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    want = O.grouped_bias_grad(bits, splits, E)
+    got = host(db)[:, cols]
+    for g in range(E):
+        if splits[g] == 0:
+            assert np.all(got[g] == 0), f"group {g} is empty: its bias grad must be 0"
+        else:
+            e = np.linalg.norm(got[g].astype(np.float64) - want[g]) / np.linalg.norm(want[g])
+            assert e <= REL_TOL, f"group {g}: rel err {e}"

@@ -170,3 +170,67 @@ def test_weight_cache_reused_across_microbatches_in_a_graph(kind):
             assert _same_bits(got[m][:L], want[m][:L]), f"seed {seed}: y of microbatch {m}"
             assert _same_bits(got[nmb + m][:L], want[nmb + m][:L]), f"seed {seed}: dx of microbatch {m}"
         assert _same_bits(got[-1], want[-1]), f"seed {seed}: accumulated dW"
+
+
+def test_captured_fc1_chain_moe_e64_zipf():
+    """The moe_e64_zipf fc1 chain at full size (64 experts, 65536 Zipf-routed
+    tokens + 1024 garbage rows, hidden 7168, width 2048): quantise X, W and
+    dY, fprop, dgrad and a wgrad accumulating into the 3.8 GB fp32 main grad,
+    captured once and replayed.  A replay gives the eager bits for the Zipf
+    split sizes and for the same sizes in another expert order, written into
+    the same device buffer between replays."""
+    import workloads as W
+    w = W.workload("moe_e64_zipf")
+    E, R, L, H, F = w.num_groups, w.rows_cap, w.live_rows, w.hidden, w.ffn
+    rec = gq.Recipe(gq.RECIPE_MXFP8_1X32, 1, 1, 0.0)
+    bf = torch.bfloat16
+    x = W.device_activation(w, H, 90, device=DEV)
+    dy = W.device_activation(w, F, 91, device=DEV)
+    wt = W.device_normal_bf16((E * F, H), w.seed, 0.02, 92, DEV)
+    dw0 = W.device_normal_bf16((E, F, H), w.seed, 1e-3, 93, DEV).float()
+    qx = gq.alloc_quantized(R, H, E, rec, DEV)
+    qw = gq.alloc_quantized(E * F, H, E, rec, DEV)
+    qd = gq.alloc_quantized(R, F, E, rec, DEV)
+    y = torch.empty((R, F), dtype=bf, device=DEV)
+    dx = torch.empty((R, H), dtype=bf, device=DEV)
+    dw = torch.empty_like(dw0)
+    sp = torch.zeros(E, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(gq.WGRAD_WORKSPACE_BYTES, dtype=torch.uint8, device=DEV)
+    orders = [np.asarray(w.splits, np.int32),
+              np.asarray(w.splits, np.int32)[np.random.default_rng(94).permutation(E)]]
+
+    def chain():
+        gq.gq_quantize(x, sp, E, rec, qx, st)
+        gq.gq_quantize(wt, None, E, rec, qw, st)
+        gq.gq_quantize(dy, sp, E, rec, qd, st)
+        gq.gq_gemm_fprop(qx, qw, sp, E, F, H, y, gq.DTYPE_BF16, st)
+        gq.gq_gemm_dgrad(qd, qw, sp, E, F, H, dx, gq.DTYPE_BF16, st)
+        gq.gq_gemm_wgrad(qd, qx, sp, E, F, H, dw, True, st, workspace=ws)
+
+    def reset(splits):
+        sp.copy_(torch.from_numpy(splits))
+        dw.copy_(dw0)
+        y.fill_(float("nan"))
+        dx.fill_(float("nan"))
+
+    reset(orders[0])
+    chain()                                   # first calls on the device: set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        chain()
+    for trial, splits in enumerate(orders):
+        reset(splits)
+        graph.replay()
+        torch.cuda.synchronize()
+        check_status(st)
+        got = (y.clone(), dx.clone(), dw.clone())
+        reset(splits)
+        chain()
+        torch.cuda.synchronize()
+        check_status(st)
+        for name, g, e in zip(("y", "dx", "dw"), got, (y, dx, dw)):
+            assert _same_bits(g, e), f"order {trial}: {name} differs from the eager result"
+        assert not torch.isnan(got[0][:L].float()).any()
+        assert torch.isnan(got[0][L:].float()).all()
