@@ -128,13 +128,16 @@ constexpr int kWgSlots = GQ_WG_SLOTS;
 // warp's share is four 32-column boxes; either all four go by load + add +
 // store, or boxes 1 and 3 go by TMA reduce-add and the others by load + add
 // + store.  Measured on a 3.8 GB fp32 buffer: when every SM carries main-grad
-// traffic, load + add + store alone reaches the copy rate and the mix falls
+// traffic, load + add + store alone reaches the copy rate and mixes fall
 // short of it; when only half of the SMs do (the others busy with long
 // contractions), load + add + store alone and reduce-add alone each move
-// about 70% of the copy rate and the mix about 100%, because the reduce-adds
-// hold no load in flight.  So the kernel mixes when the split sizes are
-// skewed: when the largest group holds at least GQ_WG_MIX_SKEW times the
-// mean live group (tuning knob; 0 = always mix, a huge value = never).
+// about 70% of the copy rate and mixes more (the reduce-adds hold no load in
+// flight): 79% with half the boxes by reduce-add, ~100% with 10-12 of 16.  In
+// the kernel itself, beside the long contractions, half is the fastest share
+// (one or three boxes in four by reduce-add are slower).  So the kernel mixes
+// when the split sizes are skewed: when the largest group holds at least
+// GQ_WG_MIX_SKEW times the mean live group (tuning knob; 0 = always mix, a
+// huge value = never).
 #ifndef GQ_WG_MIX_SKEW
 #define GQ_WG_MIX_SKEW 4
 #endif
