@@ -102,7 +102,8 @@ typedef enum gq_dtype { GQ_DTYPE_F32 = 0, GQ_DTYPE_BF16 = 1 } gq_dtype;
 
 typedef struct gq_recipe {
     int32_t kind;        /* gq_recipe_kind */
-    int32_t rowwise;     /* 1: produce rowwise codes + scales (MX only) */
+    int32_t rowwise;     /* 1: produce rowwise codes + scales (MX and NVFP4; the
+                            per-channel recipe is columnwise only) */
     int32_t colwise;     /* 1: produce columnwise codes + scales */
     float zero_scale;    /* per-channel recipe: the scale of an all-zero block (the
                             page's sf_val); ignored by MX */
